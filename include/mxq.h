@@ -1,0 +1,193 @@
+/*
+ * mxq.h -- C ABI of libmxq, the GB300 (sm_103a) MXFP8 activation chain.
+ *
+ * The operations follow two vLLM pull-request pages:
+ *   [MegaAttn]  "[Perf][DSv4.1] MegaAttn: wo_a writes wo_b's MXFP8 input" (vllm#60118)
+ *   [KeepMXFP8] "[Perf][DSv4.1] Keep activations MXFP8 between DeepGEMM kernels" (vllm#57977)
+ *
+ * MXFP8 here means: E4M3 values (OCP FP8, "FN" variant, largest finite 448) with one UE8M0
+ * scale byte b (value 2^(b-127)) per 32 consecutive elements along the contraction / row
+ * dimension K ([KeepMXFP8] review: "1 scale per 32 elements along K"). For a group with
+ * largest magnitude amax the scale 2^e is the smallest power of two with amax / 2^e <= 448
+ * (never below 2^-127; an all-zero group takes byte 0), and each element x is stored as the
+ * E4M3 value nearest to x * 2^-e (round to nearest, ties to even, saturating at +-448; the
+ * sign of a zero result follows x).
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller. The library never
+ *     allocates, frees or synchronizes inside a compute call; work is enqueued on `stream`
+ *     (a cudaStream_t passed as void*, NULL = the legacy default stream) and returns at once.
+ *   - bf16 is IEEE binary32's upper half; E4M3 and UE8M0 are bytes.
+ *   - Row strides (ld*) are in ELEMENTS of the tensor's type; every pointer and every row
+ *     stride in bytes must be a multiple of 16.
+ *   - Argument errors are detected on the host before anything is launched and return a
+ *     status other than MXQ_OK; the outputs are then untouched.
+ *   - Launch failures return MXQ_ERR_CUDA (cudaGetLastError after the launch).
+ *   - Device-side bounded waits that give up (a pipeline stalled for about a second) record
+ *     MXQ_ERR_TIMEOUT in the optional `status` word and end the kernel cleanly; read it with
+ *     mxq_check_status. Outputs of such a call are undefined.
+ *   - Inputs must be finite (NaN/Inf are outside the contract).
+ *
+ * Scale-factor layouts (the pages name them -- "F8_128x4", "int32-packed", "MN-major" -- but do
+ * not print them; these are the byte layouts this library reads and writes):
+ *   MXQ_SF_ROWMAJOR_U8   : byte sf[m * Kg + g], Kg = K/32.
+ *   MXQ_SF_PACKED_I32_MN : uint32 words, word w of row m holds groups 4w..4w+3 (group 4w+j in
+ *                          byte j, little-endian); stored packed[w * Mp + m], Mp = ceil(M/4)*4;
+ *                          requires K % 128 == 0. Padding rows hold 0.
+ *   MXQ_SF_TILED_128X4   : rows padded to Mp = ceil(M/128)*128, groups to Gp = ceil(Kg/4)*4;
+ *                          512-byte tiles of 128 rows x 4 groups in row-tile-major order; row r,
+ *                          group c of a tile at byte (r % 32) * 16 + (r / 32) * 4 + c. This is
+ *                          the block-scale layout the tensor cores read. Padding holds 0.
+ * Buffer sizes: mxq_sf_bytes().
+ */
+#ifndef MXQ_H_
+#define MXQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MXQ_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define MXQ_API __attribute__((visibility("default")))
+#else
+#define MXQ_API
+#endif
+
+typedef enum mxq_status {
+  MXQ_OK = 0,
+  MXQ_ERR_INVALID_ARG = 1,       /* required pointer NULL, size <= 0, bad layout tag value  */
+  MXQ_ERR_UNSUPPORTED_SHAPE = 2, /* K % 32 != 0, packed scales with K % 128 != 0, a GEMM
+                                    dimension outside the kernels' tiling (see each call)     */
+  MXQ_ERR_MISALIGNED = 3,        /* a pointer or a row stride in bytes not a multiple of 16   */
+  MXQ_ERR_LAYOUT = 4,            /* scale layout tag not accepted by this call               */
+  MXQ_ERR_CUDA = 5,              /* CUDA error on the host side (launch, attribute, device)  */
+  MXQ_ERR_TIMEOUT = 6            /* a device-side bounded wait gave up (from the status word) */
+} mxq_status;
+
+typedef enum mxq_sf_layout {
+  MXQ_SF_ROWMAJOR_U8 = 0,
+  MXQ_SF_PACKED_I32_MN = 1,
+  MXQ_SF_TILED_128X4 = 2
+} mxq_sf_layout;
+
+/* An MXFP8 operand: E4M3 bytes [rows, cols] row-major with row stride `ld` bytes, and its
+ * UE8M0 scales in `sf_layout` (the layout tag keeps producers and consumers of different
+ * scale layouts from being mixed, as [KeepMXFP8] "Pieces" requires of its QuantKey). */
+typedef struct mxq_mx_tensor {
+  const void* data;
+  const void* sf;
+  int32_t sf_layout;
+  int64_t rows;
+  int64_t cols;
+  int64_t ld;
+} mxq_mx_tensor;
+
+/* ABI version of the loaded library (MXQ_ABI_VERSION at build time). */
+MXQ_API int mxq_abi_version(void);
+
+/* Static, NUL-terminated name of a status code. */
+MXQ_API const char* mxq_status_string(mxq_status s);
+
+/* Name of the CUDA error behind the last MXQ_ERR_CUDA returned on the calling thread. */
+MXQ_API const char* mxq_last_error_string(void);
+
+/* Bytes of a scale buffer in `layout` for an [M, K] MXFP8 tensor; 0 if the shape is invalid
+ * for that layout (K % 32 != 0, or packed with K % 128 != 0). */
+MXQ_API size_t mxq_sf_bytes(int32_t layout, int64_t M, int64_t K);
+
+/* Bytes of the optional device status word that the GEMM calls accept (zero it before use). */
+MXQ_API size_t mxq_status_bytes(void);
+
+/* Synchronizes `stream`, then reads the device status word written by earlier calls:
+ * MXQ_OK if no bounded wait gave up, MXQ_ERR_TIMEOUT otherwise, MXQ_ERR_CUDA on a CUDA error.
+ * This is the only call that synchronizes. */
+MXQ_API mxq_status mxq_check_status(const void* status, void* stream);
+
+/*
+ * mxfp8_quantize -- the standalone MXFP8 quantize launch ([MegaAttn] Claims: the
+ * "mxfp8_quantize kernel" that the fused path drops; [KeepMXFP8] Purpose: the "[q]" launch).
+ *
+ *   x_bf16       : [M, K] bf16, row stride ldx elements (ldx >= K).
+ *   q_e4m3       : [M, K] E4M3 out, row stride ldq bytes (ldq >= K).
+ *   sf_rowmajor  : MXQ_SF_ROWMAJOR_U8 scales out, or NULL.
+ *   sf_packed_i32: MXQ_SF_PACKED_I32_MN scales out (K % 128 == 0), or NULL.
+ *   sf_128x4     : MXQ_SF_TILED_128X4 scales out, or NULL.
+ * Any subset of the three scale layouts is written in the same pass (at least one).
+ * Requires M >= 1, K >= 32, K % 32 == 0, M * K < 2^40.
+ */
+MXQ_API mxq_status mxfp8_quantize(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, void* q_e4m3,
+                                  int64_t ldq, void* sf_rowmajor, void* sf_packed_i32, void* sf_128x4,
+                                  void* stream);
+
+/*
+ * rmsnorm_dual_out -- RMSNorm that writes bf16 and MXFP8 at once ([KeepMXFP8] Purpose:
+ * "mega_mhc (post+pre+RMSNorm)" emitting bf16 plus "(y_fp8, y_gemm_sf)"; only the RMSNorm part).
+ *
+ *   y[t, j] = RNE_bf16( (x[t, j] * r_t) * gamma[j] ),  r_t = 1 / sqrt(mean_j x[t, j]^2 + eps)
+ * computed in fp32; (y_q, scales) = mxfp8_quantize(y) applied to that bf16 y (bit-identical).
+ *
+ *   x_bf16 [T, H] (row stride ldx), gamma_bf16 [H], y_bf16 [T, H] out (row stride H),
+ *   y_q [T, H] out (row stride H bytes), y_sf_packed_i32 / y_sf_rowmajor / y_sf_128x4: scale
+ *   outputs (NULL to skip; at least one).
+ * Requires T >= 1, 32 <= H <= 16384, H % 32 == 0 (H % 128 == 0 for the packed layout).
+ */
+MXQ_API mxq_status rmsnorm_dual_out(const void* x_bf16, const void* gamma_bf16, float eps, int64_t T,
+                                    int64_t H, int64_t ldx, void* y_bf16, void* y_q,
+                                    void* y_sf_packed_i32, void* y_sf_rowmajor, void* y_sf_128x4,
+                                    void* stream);
+
+/*
+ * wo_a_einsum_mxfp8 -- the grouped wo_a einsum of DeepSeek-V4.1's _o_proj ([MegaAttn]
+ * Validation: "8 groups x 4096 -> 1024"), read as tgk,gnk->tgn:
+ *   z[t, g*Na + n] = sum_k deq(o)[t, g*Ka + k] * deq(wa)[g*Na + n, k]   (fp32 accumulation)
+ * with the fused epilogue of [MegaAttn] Overview/Details: the fp32 result is rounded to bf16
+ * and that bf16 z is quantized to MXFP8 in registers (scales in F8_128x4), so no standalone
+ * quantize launch is needed. Bytes and scales equal mxfp8_quantize(z_bf16) of the same call.
+ *
+ *   o  : [T, G*Ka] MXFP8, sf_layout MXQ_SF_TILED_128X4 (scales over the [T, G*Ka] matrix).
+ *   wa : [G*Na, Ka] MXFP8, sf_layout MXQ_SF_TILED_128X4.
+ *   z_q, z_sf_128x4 : MXFP8 z out ([T, G*Na], row stride G*Na bytes) -- both or neither.
+ *   z_sf_packed_i32 : optional second scale layout for z (MXQ_SF_PACKED_I32_MN), or NULL.
+ *   z_bf16          : optional bf16 z out ([T, G*Na], row stride G*Na) -- the pre-fusion
+ *                     "bf16 z" output, used for validation and the unfused arm; or NULL.
+ *   status          : optional device status word (mxq_status_bytes()), or NULL.
+ * At least one of z_q / z_bf16. Requires Ka % 128 == 0, Na % 128 == 0, G >= 1, T >= 1.
+ */
+MXQ_API mxq_status wo_a_einsum_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, int64_t T,
+                                     int32_t G, int32_t Na, int32_t Ka, void* z_q, void* z_sf_128x4,
+                                     void* z_sf_packed_i32, void* z_bf16, void* status, void* stream);
+
+/*
+ * gemm_mxfp8_bf16 -- the wo_b MXFP8 GEMM ([MegaAttn] Validation: "wo_b 8192 -> 5120"; it
+ * "takes the QuantizedActivation directly"):
+ *   out[m, n] = RNE_bf16( sum_k deq(a)[m, k] * deq(b)[n, k] )   (fp32 accumulation)
+ *   a : [M, K] MXFP8 activations, b : [N, K] MXFP8 weights, both MXQ_SF_TILED_128X4.
+ *   out_bf16 : [M, N] bf16, row stride ldo elements.
+ * Requires K % 128 == 0, N % 128 == 0, M >= 1.
+ */
+MXQ_API mxq_status gemm_mxfp8_bf16(const mxq_mx_tensor* a, const mxq_mx_tensor* b, int64_t M, int64_t N,
+                                   int64_t K, void* out_bf16, int64_t ldo, void* status, void* stream);
+
+/*
+ * o_proj_mxfp8 -- the fused _o_proj pair ([MegaAttn] Overview): wo_a_einsum_mxfp8 writes z as
+ * MXFP8 with F8_128x4 scales, and gemm_mxfp8_bf16 consumes that z directly:
+ *   out = wo_b( MXFP8( RNE_bf16( einsum(o, wa) ) ) )
+ * Two kernel launches, no standalone quantize launch. Arguments as in the two calls above;
+ * z_q / z_sf_128x4 are required (the hand-off buffers), z_sf_packed_i32 and z_bf16 optional.
+ * out_bf16 : [T, Nb], row stride Nb. Requires Nb % 128 == 0.
+ */
+MXQ_API mxq_status o_proj_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, const mxq_mx_tensor* wb,
+                                int64_t T, int32_t G, int32_t Na, int32_t Ka, int32_t Nb, void* z_q,
+                                void* z_sf_128x4, void* z_sf_packed_i32, void* z_bf16, void* out_bf16,
+                                void* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXQ_H_ */

@@ -1,0 +1,194 @@
+// C ABI of libmxq: argument checks on the host, then the kernel launches of mxq_internal.h.
+// The operations and their sources are documented in include/mxq.h.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "mxq.h"
+#include "mxq_internal.h"
+
+namespace {
+
+thread_local char g_last_error[128] = "no error";
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+mxq_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return MXQ_OK;
+  std::strncpy(g_last_error, cudaGetErrorName(e), sizeof(g_last_error) - 1);
+  g_last_error[sizeof(g_last_error) - 1] = '\0';
+  return MXQ_ERR_CUDA;
+}
+
+// An MXFP8 GEMM operand: [rows, cols] E4M3 with F8_128x4 scales.
+mxq_status check_operand(const mxq_mx_tensor* t, int64_t rows, int64_t cols) {
+  if (t == nullptr || t->data == nullptr || t->sf == nullptr) return MXQ_ERR_INVALID_ARG;
+  if (t->sf_layout != MXQ_SF_TILED_128X4) return MXQ_ERR_LAYOUT;
+  if (t->rows != rows || t->cols != cols || t->ld < cols) return MXQ_ERR_UNSUPPORTED_SHAPE;
+  if (!al16(t->data) || !al16(t->sf) || (t->ld % 16) != 0) return MXQ_ERR_MISALIGNED;
+  if (t->ld >= (int64_t(1) << 40) || rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31))
+    return MXQ_ERR_UNSUPPORTED_SHAPE;
+  return MXQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mxq_abi_version(void) { return MXQ_ABI_VERSION; }
+
+const char* mxq_status_string(mxq_status s) {
+  switch (s) {
+    case MXQ_OK: return "MXQ_OK";
+    case MXQ_ERR_INVALID_ARG: return "MXQ_ERR_INVALID_ARG";
+    case MXQ_ERR_UNSUPPORTED_SHAPE: return "MXQ_ERR_UNSUPPORTED_SHAPE";
+    case MXQ_ERR_MISALIGNED: return "MXQ_ERR_MISALIGNED";
+    case MXQ_ERR_LAYOUT: return "MXQ_ERR_LAYOUT";
+    case MXQ_ERR_CUDA: return "MXQ_ERR_CUDA";
+    case MXQ_ERR_TIMEOUT: return "MXQ_ERR_TIMEOUT";
+  }
+  return "MXQ_UNKNOWN_STATUS";
+}
+
+const char* mxq_last_error_string(void) { return g_last_error; }
+
+size_t mxq_sf_bytes(int32_t layout, int64_t M, int64_t K) {
+  if (M <= 0 || K <= 0 || K % 32 != 0) return 0;
+  const int64_t Kg = K / 32;
+  switch (layout) {
+    case MXQ_SF_ROWMAJOR_U8: return static_cast<size_t>(M * Kg);
+    case MXQ_SF_PACKED_I32_MN:
+      if (K % 128 != 0) return 0;
+      return static_cast<size_t>((Kg / 4) * cdiv(M, 4) * 4 * 4);
+    case MXQ_SF_TILED_128X4: return static_cast<size_t>(cdiv(M, 128) * 128 * cdiv(Kg, 4) * 4);
+    default: return 0;
+  }
+}
+
+size_t mxq_status_bytes(void) { return 16; }
+
+mxq_status mxq_check_status(const void* status, void* stream) {
+  mxq_status st = from_cuda(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  if (st != MXQ_OK || status == nullptr) return st;
+  int32_t code = 0;
+  st = from_cuda(cudaMemcpy(&code, status, sizeof(code), cudaMemcpyDeviceToHost));
+  if (st != MXQ_OK) return st;
+  return code == 0 ? MXQ_OK : MXQ_ERR_TIMEOUT;
+}
+
+mxq_status mxfp8_quantize(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, void* q_e4m3, int64_t ldq,
+                          void* sf_rowmajor, void* sf_packed_i32, void* sf_128x4, void* stream) {
+  if (x_bf16 == nullptr || q_e4m3 == nullptr) return MXQ_ERR_INVALID_ARG;
+  if (sf_rowmajor == nullptr && sf_packed_i32 == nullptr && sf_128x4 == nullptr) return MXQ_ERR_INVALID_ARG;
+  if (M <= 0 || K <= 0) return MXQ_ERR_INVALID_ARG;
+  if (K % 32 != 0 || ldx < K || ldq < K) return MXQ_ERR_UNSUPPORTED_SHAPE;
+  if (sf_packed_i32 != nullptr && K % 128 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
+  if (M >= (int64_t(1) << 31) || M * K >= (int64_t(1) << 40)) return MXQ_ERR_UNSUPPORTED_SHAPE;
+  if (!al16(x_bf16) || !al16(q_e4m3) || !al16(sf_rowmajor) || !al16(sf_packed_i32) || !al16(sf_128x4))
+    return MXQ_ERR_MISALIGNED;
+  if ((ldx * 2) % 16 != 0 || ldq % 16 != 0) return MXQ_ERR_MISALIGNED;
+  mxq::QuantizeLaunch l{x_bf16, M, K, ldx, q_e4m3, ldq, sf_rowmajor, sf_packed_i32, sf_128x4};
+  return from_cuda(mxq::launch_quantize(l, static_cast<cudaStream_t>(stream)));
+}
+
+mxq_status rmsnorm_dual_out(const void* x_bf16, const void* gamma_bf16, float eps, int64_t T, int64_t H, int64_t ldx,
+                            void* y_bf16, void* y_q, void* y_sf_packed_i32, void* y_sf_rowmajor, void* y_sf_128x4,
+                            void* stream) {
+  if (x_bf16 == nullptr || gamma_bf16 == nullptr || y_bf16 == nullptr || y_q == nullptr) return MXQ_ERR_INVALID_ARG;
+  if (y_sf_packed_i32 == nullptr && y_sf_rowmajor == nullptr && y_sf_128x4 == nullptr) return MXQ_ERR_INVALID_ARG;
+  if (T <= 0 || H <= 0 || !(eps >= 0.0f)) return MXQ_ERR_INVALID_ARG;
+  if (H % 32 != 0 || H > 16384 || ldx < H) return MXQ_ERR_UNSUPPORTED_SHAPE;
+  if (y_sf_packed_i32 != nullptr && H % 128 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
+  if (T >= (int64_t(1) << 31)) return MXQ_ERR_UNSUPPORTED_SHAPE;
+  if (!al16(x_bf16) || !al16(gamma_bf16) || !al16(y_bf16) || !al16(y_q) || !al16(y_sf_packed_i32) ||
+      !al16(y_sf_rowmajor) || !al16(y_sf_128x4))
+    return MXQ_ERR_MISALIGNED;
+  if ((ldx * 2) % 16 != 0) return MXQ_ERR_MISALIGNED;
+  mxq::RmsnormLaunch l{x_bf16, gamma_bf16, eps, T, H, ldx, y_bf16, y_q, y_sf_packed_i32, y_sf_rowmajor, y_sf_128x4};
+  return from_cuda(mxq::launch_rmsnorm(l, static_cast<cudaStream_t>(stream)));
+}
+
+mxq_status wo_a_einsum_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, int64_t T, int32_t G, int32_t Na,
+                             int32_t Ka, void* z_q, void* z_sf_128x4, void* z_sf_packed_i32, void* z_bf16,
+                             void* status, void* stream) {
+  if (T <= 0 || G <= 0 || Na <= 0 || Ka <= 0) return MXQ_ERR_INVALID_ARG;
+  if ((z_q == nullptr) != (z_sf_128x4 == nullptr)) return MXQ_ERR_INVALID_ARG;
+  if (z_q == nullptr && z_bf16 == nullptr) return MXQ_ERR_INVALID_ARG;
+  if (z_sf_packed_i32 != nullptr && z_q == nullptr) return MXQ_ERR_INVALID_ARG;
+  if (Na % 128 != 0 || Ka % 128 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
+  if (T >= (int64_t(1) << 31) || static_cast<int64_t>(G) * Ka >= (int64_t(1) << 31) ||
+      static_cast<int64_t>(G) * Na >= (int64_t(1) << 31))
+    return MXQ_ERR_UNSUPPORTED_SHAPE;
+  mxq_status st = check_operand(o, T, static_cast<int64_t>(G) * Ka);
+  if (st != MXQ_OK) return st;
+  if ((st = check_operand(wa, static_cast<int64_t>(G) * Na, Ka)) != MXQ_OK) return st;
+  if (!al16(z_q) || !al16(z_sf_128x4) || !al16(z_sf_packed_i32) || !al16(z_bf16) || !al16(status))
+    return MXQ_ERR_MISALIGNED;
+  mxq::GemmLaunch l = {};
+  l.act = o->data;
+  l.act_sf = o->sf;
+  l.act_cols = o->cols;
+  l.act_ld = o->ld;
+  l.act_k_per_group = Ka;
+  l.wt = wa->data;
+  l.wt_sf = wa->sf;
+  l.wt_ld = wa->ld;
+  l.T = T;
+  l.G = G;
+  l.n_feat = Na;
+  l.k_len = Ka;
+  l.out_bf16 = z_bf16;
+  l.ldo = static_cast<int64_t>(G) * Na;
+  l.z_q = z_q;
+  l.z_sf_tiled = z_sf_128x4;
+  l.z_sf_packed = z_sf_packed_i32;
+  l.status = static_cast<int32_t*>(status);
+  return from_cuda(mxq::launch_gemm(l, static_cast<cudaStream_t>(stream)));
+}
+
+mxq_status gemm_mxfp8_bf16(const mxq_mx_tensor* a, const mxq_mx_tensor* b, int64_t M, int64_t N, int64_t K,
+                           void* out_bf16, int64_t ldo, void* status, void* stream) {
+  if (M <= 0 || N <= 0 || K <= 0 || out_bf16 == nullptr) return MXQ_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 128 != 0 || ldo < N) return MXQ_ERR_UNSUPPORTED_SHAPE;
+  mxq_status st = check_operand(a, M, K);
+  if (st != MXQ_OK) return st;
+  if ((st = check_operand(b, N, K)) != MXQ_OK) return st;
+  if (!al16(out_bf16) || !al16(status) || (ldo * 2) % 16 != 0) return MXQ_ERR_MISALIGNED;
+  mxq::GemmLaunch l = {};
+  l.act = a->data;
+  l.act_sf = a->sf;
+  l.act_cols = a->cols;
+  l.act_ld = a->ld;
+  l.act_k_per_group = 0;
+  l.wt = b->data;
+  l.wt_sf = b->sf;
+  l.wt_ld = b->ld;
+  l.T = M;
+  l.G = 1;
+  l.n_feat = static_cast<int32_t>(N);
+  l.k_len = static_cast<int32_t>(K);
+  l.out_bf16 = out_bf16;
+  l.ldo = ldo;
+  l.status = static_cast<int32_t*>(status);
+  return from_cuda(mxq::launch_gemm(l, static_cast<cudaStream_t>(stream)));
+}
+
+mxq_status o_proj_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, const mxq_mx_tensor* wb, int64_t T,
+                        int32_t G, int32_t Na, int32_t Ka, int32_t Nb, void* z_q, void* z_sf_128x4,
+                        void* z_sf_packed_i32, void* z_bf16, void* out_bf16, void* status, void* stream) {
+  if (z_q == nullptr || z_sf_128x4 == nullptr || out_bf16 == nullptr) return MXQ_ERR_INVALID_ARG;
+  if (Nb <= 0 || G <= 0 || Na <= 0) return MXQ_ERR_INVALID_ARG;
+  if (Nb % 128 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
+  const int64_t Kb = static_cast<int64_t>(G) * Na;
+  mxq_status st = check_operand(wb, Nb, Kb);
+  if (st != MXQ_OK) return st;
+  if (!al16(out_bf16)) return MXQ_ERR_MISALIGNED;
+  st = wo_a_einsum_mxfp8(o, wa, T, G, Na, Ka, z_q, z_sf_128x4, z_sf_packed_i32, z_bf16, status, stream);
+  if (st != MXQ_OK) return st;
+  const mxq_mx_tensor z = {z_q, z_sf_128x4, MXQ_SF_TILED_128X4, T, Kb, Kb};
+  return gemm_mxfp8_bf16(&z, wb, T, Nb, Kb, out_bf16, Nb, status, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,535 @@
+// Block-scaled MXFP8 GEMMs of the _o_proj chain on 5th-generation tensor cores (sm_103a).
+//
+// Pages: "[Perf][DSv4.1] MegaAttn: wo_a writes wo_b's MXFP8 input" (Overview, Validation,
+// Details): wo_a is a grouped FP8 einsum "8 groups x 4096 -> 1024" whose epilogue writes z as
+// MXFP8 with F8_128x4 scales; wo_b is an MXFP8 GEMM "8192 -> 5120" that takes that z directly.
+//
+// One kernel template serves both. Per CTA (192 threads):
+//   warp 0      TMA producer: operand tiles (128-byte swizzle) + 512-byte scale atoms
+//   warp 1      TMEM owner and MMA issuer: tcgen05.cp copies each stage's scale atoms into
+//               TMEM, then 4 x tcgen05.mma kind::mxf8f6f4 block_scale (K = 32 each)
+//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator, bf16 rounding, and (for wo_a)
+//               per-32 MXFP8 quantization in registers
+// Two orientations:
+//   normal  (large T): A = activations (128 tokens / tile), B = weights (BN features / tile).
+//           TMEM lane = token row, so one thread holds a 32-column quantization group.
+//   swap-AB (T <= 256): A = weights (128 features / tile), B = activations (all tokens, BN).
+//           TMEM lane = feature, so a quantization group is one warp (32 lanes). The K range
+//           is split over a thread-block cluster; partial sums meet in distributed shared
+//           memory and are added in fixed rank order (deterministic, no atomics).
+// Every mbarrier wait is bounded (about 1 s); a wait that gives up records MXQ_ERR_TIMEOUT in
+// the optional status word and the CTA drains its own copies and MMAs before leaving.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "mxq_device.cuh"
+#include "mxq_internal.h"
+
+namespace mxq {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int BM = 128;            // MMA M: rows of the A operand = TMEM lanes
+constexpr int BK = 128;            // K bytes per stage = one 128-byte swizzle row
+constexpr int kStatusTimeout = 6;  // MXQ_ERR_TIMEOUT
+
+struct KArgs {
+  int64_t T;
+  int32_t n_feat;
+  int32_t kb_per_cta;       // 128-wide k-blocks per CTA
+  int32_t splits;           // swap-AB: CTAs per cluster along K
+  int64_t act_k_per_group;  // activation column offset between groups
+  const uint8_t* act_sf;
+  int64_t act_gp4;  // 512-byte atoms per activation row tile
+  const uint8_t* wt_sf;
+  int64_t wt_gp4;
+  uint16_t* out_bf16;
+  int64_t ldo;
+  uint8_t* z_q;
+  int64_t ldz;
+  uint8_t* z_sf_tl;
+  int64_t z_gp4, z_mp128;
+  uint8_t* z_sf_pk;  // byte view of the packed words
+  int64_t z_mp4;
+  int32_t* status;
+};
+
+__device__ __forceinline__ void report_timeout(int32_t* status) {
+  if (status != nullptr) atomicCAS(status, 0, kStatusTimeout);
+}
+
+template <int BN, int STAGES>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK;
+  static constexpr int B_BYTES = BN * BK;
+  static constexpr int SFB_ATOMS = (BN + 127) / 128;
+  static constexpr int SF_BYTES = 512 * (1 + SFB_ATOMS);
+  static constexpr int SF_COLS = 16;  // TMEM columns per stage slot (4 for A + 4 per B atom, padded)
+  static constexpr int TX_BYTES = A_BYTES + B_BYTES + SF_BYTES;
+  static constexpr int OFF_B = STAGES * A_BYTES;
+  static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_BAR = OFF_SF + STAGES * SF_BYTES;
+  static constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 1) * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+  static constexpr int TMEM_USED = BN + STAGES * SF_COLS;
+  static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
+                                   : TMEM_USED <= 64  ? 64
+                                   : TMEM_USED <= 128 ? 128
+                                   : TMEM_USED <= 256 ? 256
+                                                      : 512;
+  // Co-resident CTAs must never need more than the SM's 512 TMEM columns in total (a CTA
+  // blocked in tcgen05.alloc while a cluster peer waits for it would never resume), so the
+  // launch requests enough shared memory to keep at most 512 / TMEM_COLS CTAs per SM.
+  static constexpr int SM_SMEM = 228 * 1024;
+  static constexpr int MAX_CO = 512 / TMEM_COLS;
+  static constexpr int SMEM_FLOOR = SM_SMEM / (MAX_CO + 1) + 1024;
+  static constexpr int SMEM_LAUNCH = SMEM_BYTES > SMEM_FLOOR ? SMEM_BYTES : SMEM_FLOOR;
+  static constexpr int RC = BN < 128 ? BN : 128;  // split-K reduction columns per pass
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+  static_assert(TMEM_USED <= 512, "TMEM");
+  static_assert(RC * 128 * 4 <= OFF_SF, "reduction buffer must fit in the tile region");
+  static_assert(SMEM_LAUNCH <= 227 * 1024, "shared memory");
+  static_assert(4 * (1 + SFB_ATOMS) <= SF_COLS, "scale slot");
+};
+
+// ---- epilogue helpers ----------------------------------------------------------------------
+__device__ __forceinline__ uint32_t amax_bf16x2_words(const uint32_t* hb, int n) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < n; ++i) m = max(m, absmax_bf16x2(hb[i]));
+  return m;
+}
+
+// normal orientation: one thread = one token row, 32 consecutive feature columns
+__device__ __forceinline__ void epi_row_chunk(const KArgs& p, const uint32_t (&acc)[32], int64_t row, int64_t col,
+                                              uint32_t& word, int c) {
+  uint32_t hb[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) hb[i] = bf16x2_rn(__uint_as_float(acc[2 * i]), __uint_as_float(acc[2 * i + 1]));
+  const bool vrow = row < p.T;
+  if (p.out_bf16 != nullptr && vrow) {
+    uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + row * p.ldo + col);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hb[4 * i], hb[4 * i + 1], hb[4 * i + 2], hb[4 * i + 3]);
+  }
+  if (p.z_q != nullptr) {
+    const uint32_t code = ue8m0_from_bf16_amax(amax_bf16x2_words(hb, 16));
+    const float s = ue8m0_inverse(code);
+    uint32_t qw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      qw[i] = e4m3x2(bf16_lo(hb[2 * i]) * s, bf16_hi(hb[2 * i]) * s) |
+              (e4m3x2(bf16_lo(hb[2 * i + 1]) * s, bf16_hi(hb[2 * i + 1]) * s) << 16);
+    if (vrow) {
+      uint4* dst = reinterpret_cast<uint4*>(p.z_q + row * p.ldz + col);
+      dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+      dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+    }
+    word |= code << (8 * (c & 3));
+    if ((c & 3) == 3) {
+      const int64_t wi = (col - 96) >> 7;  // first column of this 4-group word / 128
+      if (p.z_sf_tl != nullptr)
+        *reinterpret_cast<uint32_t*>(p.z_sf_tl + tiled128x4_word_offset(row, wi, p.z_gp4)) = word;
+      if (p.z_sf_pk != nullptr && row < p.z_mp4)
+        *reinterpret_cast<uint32_t*>(p.z_sf_pk + (wi * p.z_mp4 + row) * 4) = word;
+      word = 0;
+    }
+  }
+}
+
+// swap orientation: one warp = 32 consecutive features (one quantization group), one token
+__device__ __forceinline__ void epi_feature_token(const KArgs& p, float v, int64_t t, int64_t col, int lane) {
+  const uint32_t hb = bf16x2_rn(v, 0.f) & 0xFFFFu;
+  const bool vt = t < p.T;
+  if (p.out_bf16 != nullptr && vt) p.out_bf16[t * p.ldo + col] = static_cast<uint16_t>(hb);
+  if (p.z_q != nullptr) {
+    const uint32_t amax = __reduce_max_sync(0xffffffffu, hb & 0x7FFFu);
+    const uint32_t code = ue8m0_from_bf16_amax(amax);
+    const uint32_t byte = e4m3x2(bf16_lo(hb) * ue8m0_inverse(code), 0.f) & 0xFFu;
+    if (vt) p.z_q[t * p.ldz + col] = static_cast<uint8_t>(byte);
+    if (lane == 0) {
+      const int64_t gi = col >> 5;
+      if (p.z_sf_tl != nullptr)
+        p.z_sf_tl[tiled128x4_word_offset(t, gi >> 2, p.z_gp4) + (gi & 3)] = static_cast<uint8_t>(code);
+      if (p.z_sf_pk != nullptr && t < p.z_mp4)
+        p.z_sf_pk[((gi >> 2) * p.z_mp4 + t) * 4 + (gi & 3)] = static_cast<uint8_t>(code);
+    }
+  }
+}
+
+template <int BN, int STAGES, bool SWAP>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                     const KArgs p) {
+  using C = Cfg<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t sraw = smem_u32(smem_raw);
+  const uint32_t sbase = (sraw + 1023u) & ~1023u;  // 128-byte-swizzled tiles need 1024-byte alignment
+  uint8_t* smem = smem_raw + (sbase - sraw);
+  const uint32_t bar_full = sbase + C::OFF_BAR;      // STAGES x 8 B
+  const uint32_t bar_empty = bar_full + STAGES * 8;  // STAGES x 8 B
+  const uint32_t bar_accf = bar_empty + STAGES * 8;  // 8 B
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  int* issued_cnt = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
+  int* consumed_cnt = reinterpret_cast<int*>(smem + C::OFF_MISC + 12);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- tile coordinates ----
+  int g, split;
+  int64_t a_row0, b_row0, a_xoff, b_xoff, a_rt, b_rt0, a_kc0, b_kc0;
+  const uint8_t *a_sf, *b_sf;
+  int64_t a_gp4, b_gp4;
+  int64_t m0;  // first A row of this tile inside its group (features in swap, tokens otherwise)
+  if (SWAP) {
+    g = blockIdx.z / p.splits;
+    split = blockIdx.z % p.splits;
+    m0 = static_cast<int64_t>(blockIdx.x) * BM;
+    a_row0 = static_cast<int64_t>(g) * p.n_feat + m0;  // weights
+    b_row0 = 0;                                        // activations
+    a_xoff = 0;
+    b_xoff = static_cast<int64_t>(g) * p.act_k_per_group;
+    a_sf = p.wt_sf;
+    a_gp4 = p.wt_gp4;
+    a_rt = a_row0 >> 7;
+    a_kc0 = 0;
+    b_sf = p.act_sf;
+    b_gp4 = p.act_gp4;
+    b_rt0 = 0;
+    b_kc0 = b_xoff >> 7;
+  } else {
+    g = blockIdx.z;
+    split = 0;
+    m0 = static_cast<int64_t>(blockIdx.y) * BM;
+    a_row0 = m0;                                                                          // activations
+    b_row0 = static_cast<int64_t>(g) * p.n_feat + static_cast<int64_t>(blockIdx.x) * BN;  // weights
+    a_xoff = static_cast<int64_t>(g) * p.act_k_per_group;
+    b_xoff = 0;
+    a_sf = p.act_sf;
+    a_gp4 = p.act_gp4;
+    a_rt = a_row0 >> 7;
+    a_kc0 = a_xoff >> 7;
+    b_sf = p.wt_sf;
+    b_gp4 = p.wt_gp4;
+    b_rt0 = b_row0 >> 7;
+    b_kc0 = 0;
+  }
+  const int kb_begin = split * p.kb_per_cta;
+  const int nk = p.kb_per_cta;
+
+  // ---- setup ----
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_b);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_accf, 1);
+    *abort_flag = 0;
+    *issued_cnt = 0;
+    *consumed_cnt = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // ---- roles ----
+  if (warp == 0 && lane == 0) {
+    int i = 0;
+    for (; i < nk; ++i) {
+      const int s = i % STAGES;
+      const uint32_t ph = (i / STAGES) & 1;
+      if (*abort_flag) break;
+      if (!mbar_wait_bounded(bar_empty + 8 * s, ph ^ 1)) {
+        *abort_flag = 1;
+        report_timeout(p.status);
+        break;
+      }
+      const int kb = kb_begin + i;
+      const uint32_t fb = bar_full + 8 * s;
+      mbar_arrive_expect_tx(fb, C::TX_BYTES);
+      tma_load_2d(sbase + s * C::A_BYTES, &tm_a, fb, static_cast<int32_t>(a_xoff + kb * BK),
+                  static_cast<int32_t>(a_row0));
+      tma_load_2d(sbase + C::OFF_B + s * C::B_BYTES, &tm_b, fb, static_cast<int32_t>(b_xoff + kb * BK),
+                  static_cast<int32_t>(b_row0));
+      const uint32_t sf_dst = sbase + C::OFF_SF + s * C::SF_BYTES;
+      bulk_load(sf_dst, a_sf + (a_rt * a_gp4 + a_kc0 + kb) * 512, 512, fb);
+#pragma unroll
+      for (int j = 0; j < C::SFB_ATOMS; ++j)
+        bulk_load(sf_dst + 512 * (1 + j), b_sf + ((b_rt0 + j) * b_gp4 + b_kc0 + kb) * 512, 512, fb);
+    }
+    *issued_cnt = i;
+  } else if (warp == 1 && lane == 0) {
+    int i = 0;
+    for (; i < nk; ++i) {
+      const int s = i % STAGES;
+      const uint32_t ph = (i / STAGES) & 1;
+      if (*abort_flag) break;
+      if (!mbar_wait_bounded(bar_full + 8 * s, ph)) {
+        *abort_flag = 1;
+        report_timeout(p.status);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sf_src = sbase + C::OFF_SF + s * C::SF_BYTES;
+      const uint32_t sfa_t = tmem + BN + s * C::SF_COLS;
+      const uint32_t sfb_t = sfa_t + 4;
+      tc_cp_sf_atom(sfa_t, sdesc_sf_atom(sf_src));
+#pragma unroll
+      for (int j = 0; j < C::SFB_ATOMS; ++j) tc_cp_sf_atom(sfb_t + 4 * j, sdesc_sf_atom(sf_src + 512 * (1 + j)));
+      const uint64_t ad = sdesc_kmajor_sw128(sbase + s * C::A_BYTES);
+      const uint64_t bd = sdesc_kmajor_sw128(sbase + C::OFF_B + s * C::B_BYTES);
+#pragma unroll
+      for (int k = 0; k < BK / 32; ++k)
+        tc_mma_mxf8(tmem, ad + 2 * k, bd + 2 * k, idesc_mxf8(BM, BN, k, k), sfa_t, sfb_t, (i | k) != 0 ? 1u : 0u);
+      tc_commit(bar_empty + 8 * s);
+    }
+    *consumed_cnt = i;
+    tc_commit(bar_accf);  // arrives once every MMA above has completed
+  }
+  __syncwarp();
+
+  // ---- epilogue ----
+  const bool epi = warp >= 2;
+  const int q = warp & 3;  // TMEM lane quarter this warp may access
+  const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16);
+  if (epi) {
+    if (!mbar_wait_bounded(bar_accf, 0)) {
+      *abort_flag = 1;
+      report_timeout(p.status);
+    }
+    tc_fence_after();
+  }
+
+  if (!SWAP) {
+    if (epi && !__any_sync(0xffffffffu, *abort_flag)) {
+      const int64_t row = m0 + 32 * q + lane;
+      const int64_t col0 = static_cast<int64_t>(g) * p.n_feat + static_cast<int64_t>(blockIdx.x) * BN;
+      uint32_t word = 0;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t acc[32];
+        tmem_ld_x32(t_lane + 32 * c, acc);
+        tmem_ld_wait();
+        epi_row_chunk(p, acc, row, col0 + 32 * c, word, c);
+      }
+    }
+  } else if (p.splits == 1) {
+    if (epi && !__any_sync(0xffffffffu, *abort_flag)) {
+      const int64_t col = static_cast<int64_t>(g) * p.n_feat + m0 + 32 * q + lane;
+#pragma unroll 1
+      for (int c = 0; c < BN / 16; ++c) {
+        uint32_t acc[16];
+        tmem_ld_x16(t_lane + 16 * c, acc);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) epi_feature_token(p, __uint_as_float(acc[j]), 16 * c + j, col, lane);
+      }
+    }
+  } else {
+    // split-K over the cluster: partials -> own smem [col][128 features] fp32, then rank r sums
+    // its share of the columns from every rank's buffer in rank order.
+    const uint32_t rank = cluster_ctarank();
+    const int per_rank = C::RC / p.splits;
+    const int64_t col = static_cast<int64_t>(g) * p.n_feat + m0 + 32 * q + lane;
+    const uint32_t red = sbase;  // reuses the tile region: all copies and MMAs are complete
+#pragma unroll 1
+    for (int pass = 0; pass < BN / C::RC; ++pass) {
+      if (epi && !__any_sync(0xffffffffu, *abort_flag)) {
+#pragma unroll 1
+        for (int c = 0; c < C::RC / 16; ++c) {
+          uint32_t acc[16];
+          tmem_ld_x16(t_lane + pass * C::RC + 16 * c, acc);
+          tmem_ld_wait();
+          float* dst = reinterpret_cast<float*>(smem) + (16 * c) * 128 + 32 * q + lane;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) dst[j * 128] = __uint_as_float(acc[j]);
+        }
+      }
+      cluster_sync_all();
+      if (epi && !__any_sync(0xffffffffu, *abort_flag)) {
+#pragma unroll 1
+        for (int j = 0; j < per_rank; ++j) {
+          const int tl = static_cast<int>(rank) * per_rank + j;  // column inside this pass
+          const uint32_t off = red + static_cast<uint32_t>((tl * 128 + 32 * q + lane) * 4);
+          float v = ld_dsmem_f32(mapa_shared(off, 0));
+          for (int r = 1; r < p.splits; ++r) v += ld_dsmem_f32(mapa_shared(off, static_cast<uint32_t>(r)));
+          epi_feature_token(p, v, pass * C::RC + tl, col, lane);
+        }
+      }
+      cluster_sync_all();
+    }
+  }
+
+  // swap orientation: tiled z scales of padding token rows [BN, ceil(T/128)*128) are zero
+  if (SWAP && epi && p.z_sf_tl != nullptr && split == 0) {
+    const int64_t wi = (static_cast<int64_t>(g) * p.n_feat + m0) >> 7;
+    for (int64_t t = BN + (static_cast<int>(threadIdx.x) - 64); t < p.z_mp128; t += 128)
+      *reinterpret_cast<uint32_t*>(p.z_sf_tl + tiled128x4_word_offset(t, wi, p.z_gp4)) = 0u;
+  }
+
+  // ---- teardown: drain own copies / MMAs if a wait gave up, then free TMEM ----
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    if (warp == 0 && lane == 0) {
+      for (int i = *consumed_cnt; i < *issued_cnt; ++i)
+        (void)mbar_wait_bounded(bar_full + 8 * (i % STAGES), (i / STAGES) & 1);
+    }
+    if (warp == 1 && lane == 0) (void)mbar_wait_bounded(bar_accf, 0);
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D E4M3 tensor [rows, cols], row stride ld bytes; box = 128 bytes x box_rows, 128B swizzle.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+  cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n;
+}
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+template <int BN, int STAGES>
+int ctas_per_sm() {
+  using C = Cfg<BN, STAGES>;
+  const int by_smem = C::SM_SMEM / (C::SMEM_LAUNCH + 1024);
+  const int by_tmem = 512 / C::TMEM_COLS;
+  return by_smem < by_tmem ? by_smem : by_tmem;
+}
+
+template <int BN, int STAGES, bool SWAP>
+cudaError_t launch_cfg(const GemmLaunch& l, const KArgs& ka, dim3 grid, int cluster_z, cudaStream_t stream) {
+  using C = Cfg<BN, STAGES>;
+  auto kern = gemm_mxf8_kernel<BN, STAGES, SWAP>;
+  static const cudaError_t attr_err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_LAUNCH);
+  if (attr_err != cudaSuccess) return attr_err;
+  CUtensorMap tma_act, tma_wt;
+  if (!make_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, SWAP ? BN : BM)) return cudaErrorInvalidValue;
+  if (!make_map(&tma_wt, l.wt, static_cast<int64_t>(l.G) * l.n_feat, l.k_len, l.wt_ld, SWAP ? BM : BN))
+    return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_LAUNCH;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[1];
+  cfg.numAttrs = 0;
+  if (cluster_z > 1) {
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = 1;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = static_cast<unsigned>(cluster_z);
+    cfg.numAttrs = 1;
+  }
+  cfg.attrs = attrs;
+  if (SWAP) return cudaLaunchKernelEx(&cfg, kern, tma_wt, tma_act, ka);
+  return cudaLaunchKernelEx(&cfg, kern, tma_act, tma_wt, ka);
+}
+
+// Largest split of the K range (cluster size) that divides the k-blocks and the reduction
+// columns and keeps every CTA resident in one wave.
+int pick_splits(int tiles, int kb_total, int rc, int slots) {
+  for (int s = 8; s > 1; s >>= 1)
+    if (kb_total % s == 0 && rc % s == 0 && tiles * s <= slots) return s;
+  return 1;
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_swap(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
+  const int tiles = l.G * (l.n_feat / BM);
+  const int kb_total = l.k_len / BK;
+  const int slots = num_sms() * ctas_per_sm<BN, STAGES>();
+  const int s = pick_splits(tiles, kb_total, Cfg<BN, STAGES>::RC, slots);
+  ka.splits = s;
+  ka.kb_per_cta = kb_total / s;
+  dim3 grid(static_cast<unsigned>(l.n_feat / BM), 1, static_cast<unsigned>(l.G * s));
+  return launch_cfg<BN, STAGES, true>(l, ka, grid, s, stream);
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_normal(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
+  ka.splits = 1;
+  ka.kb_per_cta = l.k_len / BK;
+  dim3 grid(static_cast<unsigned>(l.n_feat / BN), static_cast<unsigned>(ceil_div(l.T, BM)),
+            static_cast<unsigned>(l.G));
+  return launch_cfg<BN, STAGES, false>(l, ka, grid, 1, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmLaunch& l, cudaStream_t stream) {
+  KArgs ka = {};
+  ka.T = l.T;
+  ka.n_feat = l.n_feat;
+  ka.act_k_per_group = l.act_k_per_group;
+  ka.act_sf = static_cast<const uint8_t*>(l.act_sf);
+  ka.act_gp4 = ceil_div(l.act_cols, 128);
+  ka.wt_sf = static_cast<const uint8_t*>(l.wt_sf);
+  ka.wt_gp4 = ceil_div(l.k_len, 128);
+  ka.out_bf16 = static_cast<uint16_t*>(l.out_bf16);
+  ka.ldo = l.ldo;
+  ka.z_q = static_cast<uint8_t*>(l.z_q);
+  ka.ldz = static_cast<int64_t>(l.G) * l.n_feat;
+  ka.z_sf_tl = static_cast<uint8_t*>(l.z_sf_tiled);
+  ka.z_gp4 = ceil_div(static_cast<int64_t>(l.G) * l.n_feat, 128);
+  ka.z_mp128 = ceil_div(l.T, 128) * 128;
+  ka.z_sf_pk = static_cast<uint8_t*>(l.z_sf_packed);
+  ka.z_mp4 = ceil_div(l.T, 4) * 4;
+  ka.status = l.status;
+  if (l.n_feat % BM != 0 || l.k_len % BK != 0) return cudaErrorInvalidValue;
+  if (l.T <= 16) return launch_swap<16, 5>(l, ka, stream);
+  if (l.T <= 32) return launch_swap<32, 4>(l, ka, stream);
+  if (l.T <= 64) return launch_swap<64, 4>(l, ka, stream);
+  if (l.T <= 128) return launch_swap<128, 3>(l, ka, stream);
+  if (l.T <= 256) return launch_swap<256, 2>(l, ka, stream);
+  if (l.n_feat % 256 == 0) return launch_normal<256, 4>(l, ka, stream);
+  return launch_normal<128, 6>(l, ka, stream);
+}
+
+}  // namespace mxq

@@ -1,0 +1,57 @@
+// Internal launcher interface of libmxq (host side). Arguments are validated by the C ABI
+// layer (api.cu) before any of these is called.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mxq {
+
+struct QuantizeLaunch {
+  const void* x;
+  int64_t M, K, ldx;
+  void* q;
+  int64_t ldq;
+  void* sf_rowmajor;
+  void* sf_packed;
+  void* sf_tiled;
+};
+cudaError_t launch_quantize(const QuantizeLaunch& a, cudaStream_t stream);
+
+struct RmsnormLaunch {
+  const void* x;
+  const void* gamma;
+  float eps;
+  int64_t T, H, ldx;
+  void* y;
+  void* yq;
+  void* sf_packed;
+  void* sf_rowmajor;
+  void* sf_tiled;
+};
+cudaError_t launch_rmsnorm(const RmsnormLaunch& a, cudaStream_t stream);
+
+// One MXFP8 GEMM of the chain, grouped over G: for group g,
+//   C_g[t, f] = sum_k deq(act)[t, g*act_k_per_group + k] * deq(wt)[g*n_feat + f, k]
+// over k < k_len; outputs at column g*n_feat + f of the bf16 and/or MXFP8 outputs.
+struct GemmLaunch {
+  const void* act;          // E4M3 [T, act_cols], row stride act_ld bytes
+  const void* act_sf;       // F8_128x4 scales of act
+  int64_t act_cols, act_ld;
+  int64_t act_k_per_group;  // column offset between groups in act (Ka for wo_a, 0 for wo_b)
+  const void* wt;           // E4M3 [G*n_feat, k_len], row stride wt_ld bytes
+  const void* wt_sf;        // F8_128x4 scales of wt
+  int64_t wt_ld;
+  int64_t T;
+  int32_t G, n_feat, k_len;
+  // outputs (any of them may be null, at least one of out_bf16 / z_q)
+  void* out_bf16;           // bf16 [T, G*n_feat] (row stride ldo elements)
+  int64_t ldo;
+  void* z_q;                // E4M3 [T, G*n_feat] (row stride G*n_feat bytes)
+  void* z_sf_tiled;         // F8_128x4 scales of z (needs z_q)
+  void* z_sf_packed;        // int32-packed MN-major scales of z (needs z_q)
+  int32_t* status;          // optional device status word
+};
+cudaError_t launch_gemm(const GemmLaunch& a, cudaStream_t stream);
+
+}  // namespace mxq
