@@ -141,20 +141,31 @@ def normal_bf16(seed: int, tid: int, nrows: int, ncols: int, std: float, rows=No
 
 
 # ---- _o_proj inputs ------------------------------------------------------------------------
+def _uniform_int(bits16: torch.Tensor, n: int) -> torch.Tensor:
+    """Map 16 random bits to an integer in [0, n) by multiply-shift (no int64 modulo)."""
+    return ((bits16 & 0xFFFF) * n) >> 16
+
+
+def _group_index(r: torch.Tensor, ngroups: int) -> torch.Tensor:
+    """[R, ngroups] global indices of the 32-element groups of rows r."""
+    return r[:, None] * ngroups + torch.arange(ngroups, dtype=torch.int64, device=r.device)[None, :]
+
+
 def o_proj_activation(seed: int, T: int, rows=None, device="cpu") -> torch.Tensor:
     """Attention output o, bf16 [T, G*KA] ~ N(0, 1); 1% of the 32-element groups (chosen by a
     hash) are multiplied by 2^k with k uniform in [-8, 8]."""
     key = stream_key(seed, TID_O)
     gkey = stream_key(seed, TID_O_GROUP)
     ncols = G * KA
+    ng = ncols // 32
 
-    def fn(idx, _r):
-        v = _to_bf16(normal(key, idx)).to(torch.float32)
-        gidx = idx // 32
+    def fn(idx, r):
+        v = _to_bf16(normal(key, idx)).to(torch.float32).view(idx.shape[0], ng, 32)
+        gidx = _group_index(r, ng)
         pick = uniform(gkey, 2 * gidx) < 0.01
-        k = (_srl(hash64(gkey, 2 * gidx + 1), 40) % 17) - 8
-        scale = torch.where(pick, torch.exp2(k.to(torch.float32)), torch.ones_like(v))
-        return (v * scale).to(torch.bfloat16)
+        k = _uniform_int(_srl(hash64(gkey, 2 * gidx + 1), 40), 17) - 8
+        scale = torch.where(pick, torch.exp2(k.to(torch.float32)), torch.ones_like(k, dtype=torch.float32))
+        return (v * scale[:, :, None]).to(torch.bfloat16).view(idx.shape[0], ncols)
 
     return _chunked_rows(T, ncols, rows, device, fn, torch.bfloat16)
 
@@ -205,32 +216,34 @@ def quantizer_input(seed: int, T: int, K: int = KB, rows=None, device="cpu") -> 
     gkey = stream_key(seed, TID_QX_GROUP)
     ekey = stream_key(seed, TID_QX_ELEM)
     assert K % 32 == 0
+    ng = K // 32
+    edge_list = [b_ for grp in EDGE_GROUPS for b_ in grp][: K]
 
     def fn(idx, r):
-        n = normal(key, idx).to(torch.float32)
-        gidx = idx // 32
-        pos = idx % 32
-        cls = uniform(gkey, 4 * gidx)
-        k = (_srl(hash64(gkey, 4 * gidx + 1), 40) % 41) - 20
-        gh = _srl(hash64(gkey, 4 * gidx + 2), 8)         # per-group bits
-        eh = _srl(hash64(ekey, idx), 8)                  # per-element bits
+        R = idx.shape[0]
+        n = normal(key, idx).to(torch.float32).view(R, ng, 32)
+        gidx = _group_index(r, ng)                                   # [R, ng]
+        cls = uniform(gkey, 4 * gidx)[:, :, None]
+        gh = _srl(hash64(gkey, 4 * gidx + 2), 8)                     # 56 per-group bits
+        k = (_uniform_int(gh >> 24, 41) - 20).to(torch.float32)[:, :, None]
+        big_pos = (gh & 31)[:, :, None]
+        p = (_uniform_int(gh >> 5, 161) - 80).to(torch.int32)[:, :, None]
+        mant = torch.where(((gh >> 21) & 1) == 1, 97, 96).to(torch.int32)[:, :, None]
+        eh = _srl(hash64(ekey, idx), 8).view(R, ng, 32)               # 56 per-element bits
+        pos = torch.arange(32, dtype=torch.int64, device=idx.device)[None, None, :]
         sign = ((eh & 1) << 15).to(torch.int32)
-        base = (n * torch.exp2(k.to(torch.float32))).to(torch.bfloat16).view(torch.int16).to(torch.int32) & 0xFFFF
-        zero = sign                                       # +0 or -0
-        sub = sign | (((eh >> 1) % 127) + 1).to(torch.int32)     # exponent field 0, mantissa 1..127
+        base = (n * torch.exp2(k)).to(torch.bfloat16).view(torch.int16).to(torch.int32) & 0xFFFF
+        zero = sign                                                   # +0 or -0
+        sub = sign | torch.clamp((eh >> 1) & 127, min=1).to(torch.int32)  # exponent field 0
         mixed = torch.where(((eh >> 9) & 1) == 1, sub, base)
-        big_pos = (gh % 32)
-        big = sign | (0x7F00 + ((eh >> 1) % 128)).to(torch.int32)
+        big = sign | (0x7F00 + ((eh >> 1) & 127)).to(torch.int32)
         withbig = torch.where(pos == big_pos, big, base)
-        # boundary groups: amax = (1 + m/128) * 2^p with m in {96, 97}; others are E4M3
-        # midpoints (1 + (2j+1)/16) * 2^(b + p - 8) with b in [-6, 7] (m = 96 case: e = p - 8).
-        p = ((gh >> 5) % 161).to(torch.int32) - 80
-        mant = torch.where(((gh >> 13) & 1) == 1, 97, 96).to(torch.int32)
+        # boundary groups: amax = (1 + m/128) * 2^p with m in {96, 97}; the other elements are
+        # E4M3 midpoints (1 + (2j+1)/16) * 2^(b + p - 8), b in [-6, 7]
         amax_bits = ((p + 127) << 7) | mant
-        j = ((eh >> 1) % 8).to(torch.int32)
-        b = ((eh >> 4) % 14).to(torch.int32) - 6
-        tie_exp = b + p - 8 + 127
-        tie_bits = (tie_exp << 7) | ((2 * j + 1) << 3)
+        jj = ((eh >> 1) & 7).to(torch.int32)
+        b = (_uniform_int(eh >> 4, 14) - 6).to(torch.int32)
+        tie_bits = ((b + p - 8 + 127) << 7) | ((2 * jj + 1) << 3)
         bnd = torch.where(pos == big_pos, amax_bits, tie_bits) | sign
         out = base
         out = torch.where(cls < 0.045, bnd, out)
@@ -238,12 +251,11 @@ def quantizer_input(seed: int, T: int, K: int = KB, rows=None, device="cpu") -> 
         out = torch.where(cls < 0.03, mixed, out)
         out = torch.where(cls < 0.02, sub, out)
         out = torch.where(cls < 0.01, zero, out)
-        # row 0 carries the hand-listed edge groups
-        ng = len(EDGE_GROUPS)
-        edge = torch.tensor([b_ for grp in EDGE_GROUPS for b_ in grp], dtype=torch.int32, device=idx.device)
-        col = idx % K
-        in_edge = (r[:, None] == 0) & (col < ng * 32)
-        out = torch.where(in_edge, edge[torch.clamp(col, max=ng * 32 - 1)], out)
+        out = out.view(R, K)
+        first = torch.nonzero(r == 0).flatten()
+        if first.numel():
+            edge = torch.tensor(edge_list, dtype=torch.int32, device=idx.device)
+            out[first, : edge.numel()] = edge
         return _bits_to_bf16(out)
 
     return _chunked_rows(T, K, rows, device, fn, torch.bfloat16)

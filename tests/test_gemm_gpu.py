@@ -1,0 +1,241 @@
+"""The _o_proj GEMMs on the GPU (page "[Perf][DSv4.1] MegaAttn: wo_a writes wo_b's MXFP8 input",
+Overview / Validation / Details).
+
+  * exact small cases: integer-valued E4M3 operands make every dot product exact in fp32, so
+    the bf16 output must equal the rounded exact result bit for bit (catches any operand,
+    scale-layout or descriptor error);
+  * wo_a bf16 z within 4e-3 relative Frobenius of the fp64 oracle; the fused MXFP8 z bytes and
+    scales identical to the standalone quantizer applied to the same call's bf16 z (the pages'
+    "wo_b receives byte-identical FP8 data and scales");
+  * the whole _o_proj output within 1e-2 relative Frobenius of the oracle's own chain.
+Token counts follow the pages' tests: 1, 129, 8193 tokens and M in {1, 4, 7, 64, 300}, plus the
+decode and prefill sweeps."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import Guarded, bf16_bits, bits_to_f64, rel_fro, u8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mxq():
+    from mxfp8_activation_quant_gb300 import build
+
+    build.build()
+    import mxfp8_activation_quant_gb300 as m
+
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    m.load()
+    return m
+
+
+def gpu_mx(mxq, x_bf16):
+    q, sfs = mxq.quantize(x_bf16.cuda(), layouts=(mxq.SF_TILED_128X4,))
+    return mxq.MXFP8(q, sfs[mxq.SF_TILED_128X4])
+
+
+def int_matrix(rng, rows, cols, lo=-4, hi=4):
+    return torch.from_numpy(rng.integers(lo, hi + 1, (rows, cols)).astype(np.float32)).to(torch.bfloat16)
+
+
+# ------------------------------------------------------------------------------------------
+# exact small GEMMs (both orientations, split and unsplit K, ragged token tails)
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("T,N,K", [(1, 128, 128), (7, 128, 256), (16, 256, 512), (64, 128, 1024),
+                                   (100, 128, 256), (200, 256, 1024), (256, 128, 512), (300, 256, 256),
+                                   (384, 128, 384), (513, 256, 512)])
+def test_gemm_exact_integers(mxq, oracle, T, N, K):
+    rng = np.random.default_rng(T * 7 + N + K)
+    a = int_matrix(rng, T, K)
+    b = int_matrix(rng, N, K)
+    A, B = gpu_mx(mxq, a), gpu_mx(mxq, b)
+    out = Guarded(T * N * 2)
+    mxq.gemm_mxfp8_bf16(A, B, out.view(torch.bfloat16, (T, N)))
+    torch.cuda.synchronize()
+    assert out.intact()
+    exact = a.double().numpy() @ b.double().numpy().T
+    want = oracle.bf16_round(exact)
+    got = u8(out.body).view(np.uint16).reshape(T, N)
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} of {T * N} differ; first {bad[:4].tolist()}: " \
+                          f"got {bits_to_f64(got[tuple(bad[0])])} want {exact[tuple(bad[0])]}"
+
+
+@pytest.mark.parametrize("T", [5, 130, 260])
+def test_gemm_random_scales(mxq, oracle, T):
+    from mxfp8_activation_quant_gb300 import synth
+
+    N, K = 256, 1024
+    a = synth.quantizer_input(11, T, K=K)
+    b = synth.normal_bf16(12, 1, N, K, 0.05)
+    A, B = gpu_mx(mxq, a), gpu_mx(mxq, b)
+    out = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    mxq.gemm_mxfp8_bf16(A, B, out)
+    torch.cuda.synchronize()
+    aq, asf = oracle.quantize_bf16(bf16_bits(a))
+    bq, bsf = oracle.quantize_bf16(bf16_bits(b))
+    ref = oracle.gemm_nt(oracle.dequant(aq, asf), oracle.dequant(bq, bsf))
+    got = bits_to_f64(bf16_bits(out))
+    # fp32 accumulation + one bf16 rounding: half a bf16 ulp of each output plus fp32 sum error
+    scale = oracle.gemm_nt(np.abs(oracle.dequant(aq, asf)), np.abs(oracle.dequant(bq, bsf)))
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + scale * K * 2.0 ** -23 + 1e-30)
+
+
+# ------------------------------------------------------------------------------------------
+# small grouped einsum: fused MXFP8 epilogue == standalone quantizer on the same bf16 z
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("T", [1, 5, 129, 260])
+def test_wo_a_small_groups(mxq, oracle, T):
+    from mxfp8_activation_quant_gb300 import synth
+
+    G, Na, Ka = 2, 256, 512
+    o = synth.quantizer_input(21, T, K=G * Ka)
+    wa = synth.normal_bf16(22, 1, G * Na, Ka, 1.0 / np.sqrt(Ka))
+    O, WA = gpu_mx(mxq, o), gpu_mx(mxq, wa)
+    zq = Guarded(T * G * Na)
+    ztl = Guarded(mxq.sf_bytes(2, T, G * Na))
+    zpk = Guarded(mxq.sf_bytes(1, T, G * Na))
+    zb = Guarded(T * G * Na * 2)
+    mxq.wo_a_einsum_mxfp8(O, WA, T, G, Na, Ka, zq.view(shape=(T, G * Na)), ztl.body, zpk.body,
+                          zb.view(torch.bfloat16, (T, G * Na)))
+    torch.cuda.synchronize()
+    for g in (zq, ztl, zpk, zb):
+        assert g.intact()
+    oq, osf = oracle.quantize_bf16(bf16_bits(o))
+    wq, wsf = oracle.quantize_bf16(bf16_bits(wa))
+    z_ref = oracle.einsum_wo_a(oracle.dequant(oq, osf), oracle.dequant(wq, wsf), G)
+    z_gpu = bits_to_f64(u8(zb.body).view(np.uint16).reshape(T, G * Na))
+    assert rel_fro(z_gpu, z_ref) <= 4e-3
+    # fused quantization == standalone quantizer applied to this call's bf16 z
+    q2, sfs = mxq.quantize(zb.view(torch.bfloat16, (T, G * Na)), layouts=(1, 2))
+    torch.cuda.synchronize()
+    assert torch.equal(q2, zq.view(shape=(T, G * Na)))
+    assert torch.equal(sfs[2], ztl.body) and torch.equal(sfs[1], zpk.body)
+
+
+# ------------------------------------------------------------------------------------------
+# full DeepSeek-V4.1 _o_proj shapes
+# ------------------------------------------------------------------------------------------
+class Weights:
+    pass
+
+
+@pytest.fixture(scope="module")
+def weights(mxq, oracle):
+    from mxfp8_activation_quant_gb300 import synth
+
+    w = Weights()
+    wa = synth.wo_a_weight(0, device="cuda")
+    wb = synth.wo_b_weight(0, device="cuda")
+    w.WA, w.WB = gpu_mx(mxq, wa), gpu_mx(mxq, wb)
+    waq, wasf = oracle.quantize_bf16(bf16_bits(wa))
+    wbq, wbsf = oracle.quantize_bf16(bf16_bits(wb))
+    w.wa_d = oracle.dequant(waq, wasf)
+    w.wb_d = oracle.dequant(wbq, wbsf)
+    # the GPU quantized the same bf16 weights the oracle did (bit-exact quantizer)
+    assert np.array_equal(u8(w.WA.data), waq) and np.array_equal(u8(w.WB.data), wbq)
+    return w
+
+
+def oracle_chain(oracle, w, o_bits):
+    from mxfp8_activation_quant_gb300 import synth
+
+    oq, osf = oracle.quantize_bf16(o_bits)
+    z_ref = oracle.einsum_wo_a(oracle.dequant(oq, osf), w.wa_d, synth.G)
+    zq, zsf = oracle.quantize_bf16(oracle.bf16_round(z_ref))
+    out_ref = oracle.gemm_nt(oracle.dequant(zq, zsf), w.wb_d)
+    return z_ref, out_ref
+
+
+def run_o_proj(mxq, w, O, T, with_bf16=True):
+    from mxfp8_activation_quant_gb300 import synth
+
+    Kb = synth.KB
+    zq = torch.empty((T, Kb), dtype=torch.uint8, device="cuda")
+    ztl = mxq.empty_sf(2, T, Kb)
+    zb = torch.empty((T, Kb), dtype=torch.bfloat16, device="cuda") if with_bf16 else None
+    out = torch.empty((T, synth.NB), dtype=torch.bfloat16, device="cuda")
+    mxq.o_proj_mxfp8(O, w.WA, w.WB, T, synth.G, synth.NA, synth.KA, synth.NB, zq, ztl, out, z_bf16=zb)
+    torch.cuda.synchronize()
+    return zq, ztl, zb, out
+
+
+@pytest.mark.parametrize("T", [1, 2, 4, 7, 8, 16, 64, 128, 129, 256, 300, 384])
+def test_o_proj_decode_shapes(mxq, oracle, weights, T):
+    from mxfp8_activation_quant_gb300 import synth
+
+    o = synth.o_proj_activation(0, T)
+    O = gpu_mx(mxq, o)
+    zq, ztl, zb, out = run_o_proj(mxq, weights, O, T)
+    z_ref, out_ref = oracle_chain(oracle, weights, bf16_bits(o))
+    assert rel_fro(bits_to_f64(bf16_bits(zb)), z_ref) <= 4e-3
+    assert rel_fro(bits_to_f64(bf16_bits(out)), out_ref) <= 1e-2
+    q2, sfs = mxq.quantize(zb, layouts=(2,))
+    torch.cuda.synchronize()
+    assert torch.equal(q2, zq) and torch.equal(sfs[2], ztl)
+    # the MXFP8-only call (no bf16 z written) gives the same bytes and output
+    zq2, ztl2, _, out2 = run_o_proj(mxq, weights, O, T, with_bf16=False)
+    assert torch.equal(zq2, zq) and torch.equal(ztl2, ztl) and torch.equal(out2, out)
+
+
+@pytest.mark.parametrize("T", [512, 4096, 8193, 32768])
+def test_o_proj_prefill_sampled_rows(mxq, oracle, weights, T):
+    """Full-size prefill: the oracle checks the first and last 128-row tiles and 256 seeded
+    rows; the fused-vs-standalone identity is checked on every row."""
+    from mxfp8_activation_quant_gb300 import synth
+
+    o = synth.o_proj_activation(0, T, device="cuda")
+    rows = synth.sample_rows(0, T)
+    o_rows = synth.o_proj_activation(0, T, rows=rows)
+    assert np.array_equal(bf16_bits(o[rows.cuda()]), bf16_bits(o_rows))
+    O = gpu_mx(mxq, o)
+    del o
+    zq, ztl, zb, out = run_o_proj(mxq, weights, O, T)
+    z_ref, out_ref = oracle_chain(oracle, weights, bf16_bits(o_rows))
+    r = rows.cuda()
+    assert rel_fro(bits_to_f64(bf16_bits(zb[r])), z_ref) <= 4e-3
+    assert rel_fro(bits_to_f64(bf16_bits(out[r])), out_ref) <= 1e-2
+    q2, sfs = mxq.quantize(zb, layouts=(2,))
+    torch.cuda.synchronize()
+    assert torch.equal(q2, zq) and torch.equal(sfs[2], ztl)
+
+
+def test_o_proj_graph_replay(mxq, weights):
+    """The two-launch chain captured in a CUDA graph replays to identical bytes."""
+    from mxfp8_activation_quant_gb300 import synth
+
+    T = 129
+    O = gpu_mx(mxq, synth.o_proj_activation(1, T))
+    zq, ztl, _, out = run_o_proj(mxq, weights, O, T, with_bf16=False)
+    zq2 = torch.zeros_like(zq)
+    ztl2 = torch.zeros_like(ztl)
+    out2 = torch.zeros_like(out)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):  # warm-up on a side stream before capture
+        mxq.o_proj_mxfp8(O, weights.WA, weights.WB, T, synth.G, synth.NA, synth.KA, synth.NB, zq2, ztl2, out2)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        mxq.o_proj_mxfp8(O, weights.WA, weights.WB, T, synth.G, synth.NA, synth.KA, synth.NB, zq2, ztl2, out2)
+    zq2.zero_()
+    ztl2.zero_()
+    out2.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(zq2, zq) and torch.equal(ztl2, ztl) and torch.equal(out2, out)
+
+
+def test_status_word_stays_clear(mxq, weights):
+    from mxfp8_activation_quant_gb300 import synth
+
+    T = 16
+    O = gpu_mx(mxq, synth.o_proj_activation(2, T))
+    st = mxq.new_status()
+    zq = torch.empty((T, synth.KB), dtype=torch.uint8, device="cuda")
+    ztl = mxq.empty_sf(2, T, synth.KB)
+    out = torch.empty((T, synth.NB), dtype=torch.bfloat16, device="cuda")
+    mxq.o_proj_mxfp8(O, weights.WA, weights.WB, T, synth.G, synth.NA, synth.KA, synth.NB, zq, ztl, out, status=st)
+    mxq.check_status(st)
+    assert int(st[0]) == 0
