@@ -1,0 +1,496 @@
+"""Benchmark of the MXFP8 activation chain on GB300.
+
+One step = one pass of the whole hot path over one batch of T tokens, inputs resident in HBM:
+  rmsnorm_dual_out  x [T, 5120] -> y bf16 + y MXFP8 (int32-packed scales)
+  mxfp8_quantize    attention output o [T, 8*4096] bf16 -> MXFP8 (F8_128x4 scales)
+  wo_a einsum       o -> z MXFP8 (fused epilogue, F8_128x4 scales)   } the _o_proj pair of
+  wo_b GEMM         z -> out bf16 [T, 5120]                           } o_proj_mxfp8
+(DeepSeek-V4.1-Flash TP1 shapes from the vLLM page "[Perf][DSv4.1] MegaAttn: wo_a writes
+wo_b's MXFP8 input", Validation). L2 is flushed before every step (cold L2, as on that page);
+each kernel is timed with CUDA events on the launching stream and the flush is outside the
+events. `value` is tokens/s through the whole chain, summed over ranks (weak scaling: every
+rank runs its own replica). Per-kernel us, GB/s, TFLOP/s and roofline fractions are reported
+alongside. `--impl reference` times the CPU oracle on a bounded sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--tokens T] [--impl reference] [--sweep]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "_o_proj us/call & TFLOP/s at T=1..32768; MXFP8 quant/RMSNorm HBM GB/s"
+G, NA, KA, NB, H = 8, 1024, 4096, 5120, 5120
+KB = G * NA
+FLOP_PER_TOKEN = 2 * G * NA * KA + 2 * NB * KB
+WEIGHT_BYTES = G * NA * KA + NB * KB + (G * NA * KA + NB * KB) // 32
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ---- algorithmic bytes / flops per launch ---------------------------------------------------
+def quant_bytes(T, K, layouts=1):
+    return T * K * 2 + T * K + layouts * T * K // 32
+
+
+def rms_bytes(T, H_=H):
+    return T * H_ * 2 + T * H_ * 2 + T * H_ + T * H_ // 32 + H_ * 2
+
+
+def wo_a_bytes(T):
+    return G * NA * KA * 33 // 32 + T * G * KA * 33 // 32 + T * KB * 33 // 32
+
+
+def wo_b_bytes(T):
+    return NB * KB * 33 // 32 + T * KB * 33 // 32 + T * NB * 2
+
+
+def wo_a_flops(T):
+    return 2 * T * G * NA * KA
+
+
+def wo_b_flops(T):
+    return 2 * T * NB * KB
+
+
+# ---- clocks -----------------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---- the GPU arm -------------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import mxfp8_activation_quant_gb300 as mxq
+    from mxfp8_activation_quant_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    mxq.load()
+    T = args.tokens
+    seed = 1000 * rank
+
+    # resident inputs and weights (weights quantized once, outside any timing)
+    def mx(x):
+        q, s = mxq.quantize(x, layouts=(mxq.SF_TILED_128X4,))
+        return mxq.MXFP8(q, s[mxq.SF_TILED_128X4])
+
+    WA = mx(synth.wo_a_weight(seed, device=dev))
+    WB = mx(synth.wo_b_weight(seed, device=dev))
+    x = synth.rmsnorm_input(seed, T, device=dev)
+    gamma = synth.rmsnorm_gamma(seed, device=dev)
+    o = synth.o_proj_activation(seed, T, device=dev)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    yq = torch.empty((T, H), dtype=torch.uint8, device=dev)
+    ysf = mxq.empty_sf(mxq.SF_PACKED_I32_MN, T, H, dev)
+    oq = torch.empty((T, G * KA), dtype=torch.uint8, device=dev)
+    osf = mxq.empty_sf(mxq.SF_TILED_128X4, T, G * KA, dev)
+    O = mxq.MXFP8(oq, osf)
+    zq = torch.empty((T, KB), dtype=torch.uint8, device=dev)
+    zsf = mxq.empty_sf(mxq.SF_TILED_128X4, T, KB, dev)
+    Z = mxq.MXFP8(zq, zsf)
+    out = torch.empty((T, NB), dtype=torch.bfloat16, device=dev)
+    status = mxq.new_status(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(4 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        mxq.rmsnorm_dual_out(x, gamma, synth.RMS_EPS, y, yq, sf_packed=ysf)
+        if ev is not None:
+            ev[1].record(stream)
+        mxq.mxfp8_quantize(o, oq, None, None, osf)
+        if ev is not None:
+            ev[2].record(stream)
+        mxq.wo_a_einsum_mxfp8(O, WA, T, G, NA, KA, z_q=zq, z_sf_128x4=zsf, status=status)
+        if ev is not None:
+            ev[3].record(stream)
+        mxq.gemm_mxfp8_bf16(Z, WB, out, status=status)
+        if ev is not None:
+            ev[4].record(stream)
+
+    KERNELS_PER_STEP = 4
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        step()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with sampler:
+        for i in range(args.steps):
+            flush.fill_((i + 7) & 0xFF)  # cold L2 before every step, outside the events
+            step(evs[i])
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    mxq.check_status(status)
+
+    parts = [[evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)] for j in range(4)]
+    step_ms = [sum(parts[j][i] for j in range(4)) for i in range(args.steps)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens_per_s = world * T * args.steps / (total_ms / 1e3)
+
+    # end-to-end through the public API: pinned host inputs -> device -> chain -> host result
+    x_h = x.cpu().pin_memory()
+    o_h = o.cpu().pin_memory()
+    out_h = torch.empty((T, NB), dtype=torch.bfloat16, pin_memory=True)
+    x_d = torch.empty_like(x)
+    o_d = torch.empty_like(o)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        o_d.copy_(o_h, non_blocking=True)
+        mxq.rmsnorm_dual_out(x_d, gamma, synth.RMS_EPS, y, yq, sf_packed=ysf)
+        mxq.mxfp8_quantize(o_d, oq, None, None, osf)
+        mxq.o_proj_mxfp8(O, WA, WB, T, G, NA, KA, NB, zq, zsf, out, status=status)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_tps = world * T * args.steps / (e2e_ms / 1e3)
+
+    hbm, bf16_tf, peak_kind = load_peaks()
+    mx_tf = 2.0 * bf16_tf  # fp8 dense rate = 2x bf16 (nominal 4.5 / 2.25 PFLOP/s)
+    names = ["rmsnorm_dual_out", "mxfp8_quantize", "wo_a_fused_mxfp8", "wo_b_mxfp8"]
+    byts = [rms_bytes(T), quant_bytes(T, G * KA), wo_a_bytes(T), wo_b_bytes(T)]
+    flops = [0, 0, wo_a_flops(T), wo_b_flops(T)]
+    detail = {}
+    for j, n in enumerate(names):
+        us = 1e3 * statistics.mean(parts[j])
+        d = {"us": round(us, 3), "GB/s": round(byts[j] / us / 1e3, 1)}
+        roof_us = max(byts[j] / hbm / 1e3, flops[j] / mx_tf / 1e6) if flops[j] else byts[j] / hbm / 1e3
+        if flops[j]:
+            d["TFLOP/s"] = round(flops[j] / us / 1e6, 1)
+        d["roofline_us"] = round(roof_us, 3)
+        d["frac"] = round(roof_us / us, 4)
+        detail[n] = d
+    o_proj_us = detail["wo_a_fused_mxfp8"]["us"] + detail["wo_b_mxfp8"]["us"]
+    detail["o_proj"] = {"us_per_call": round(o_proj_us, 3),
+                        "TFLOP/s": round(FLOP_PER_TOKEN * T / o_proj_us / 1e6, 1)}
+    dom = max(range(4), key=lambda j: statistics.mean(parts[j]))
+    dom_us = 1e3 * statistics.mean(parts[dom])
+    if flops[dom] and flops[dom] / mx_tf / 1e6 >= byts[dom] / hbm / 1e3:
+        roof = {"kernel": names[dom], "bound": "tensor", "achieved": round(flops[dom] / dom_us / 1e6, 1),
+                "peak": round(mx_tf, 1), "unit": "TFLOP/s",
+                "peak_note": f"{peak_kind} bf16 burst x 2 (fp8/bf16 nominal ratio)"}
+    else:
+        roof = {"kernel": names[dom], "bound": "hbm", "achieved": round(byts[dom] / dom_us / 1e3, 1),
+                "peak": hbm, "unit": "GB/s", "peak_note": f"{peak_kind} copy bandwidth"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = TRAFFIC.get((names[dom], T))
+
+    clocks = sampler.summary()
+    res = {
+        "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/ue8m0 (fp32 accum)",
+        "data": "synthetic (seeded SplitMix64 + Box-Muller, shapes of the pages' workloads)",
+        "config": {"workload": f"MXFP8 activation chain, DeepSeek-V4.1-Flash TP1 _o_proj + RMSNorm, T={T}",
+                   "tokens": T, "wo_a": "8 groups x 4096 -> 1024", "wo_b": "8192 -> 5120", "rmsnorm_hidden": H,
+                   "l2": "flushed before every step (outside the timed events)", "parallelism": f"replicas x{world}"},
+        "parts": detail,
+        "roofline": roof,
+        "e2e": {"value": round(e2e_tps, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": x_h.numel() * 2 + o_h.numel() * 2, "d2h_bytes_per_step": out_h.numel() * 2},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clocks,
+        "wall_ms_per_step_incl_l2_flush": round(1e3 * wall / args.steps, 4),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(args, T, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+        if args.sweep:
+            sweep(args, mxq, synth, torch, dev, WA, WB)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from the committed ncu
+# captures, keyed by (kernel, tokens); None until a capture of the current kernel exists
+TRAFFIC = {}
+
+
+def sweep(args, mxq, synth, torch, dev, WA, WB):
+    """Per-config lines for the sweep tables (not the headline line): quantizer, RMSNorm, and
+    the _o_proj pair fused vs unfused (wo_a bf16 z -> standalone quantize -> wo_b)."""
+    hbm, bf16_tf, _ = load_peaks()
+    mx_tf = 2 * bf16_tf
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(4 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timeit(fn, reps=20):
+        ts = []
+        for i in range(3):
+            flush.fill_(i)
+            fn()
+        for i in range(reps):
+            flush.fill_(i)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(ts)
+
+    for T in [1, 16, 256, 4096, 32768]:
+        x = synth.quantizer_input(0, T, device=dev)
+        q = torch.empty((T, KB), dtype=torch.uint8, device=dev)
+        sf = mxq.empty_sf(2, T, KB, dev)
+        us = timeit(lambda: mxq.mxfp8_quantize(x, q, None, None, sf))
+        b = quant_bytes(T, KB)
+        print(json.dumps({"sweep": "mxfp8_quantize", "T": T, "us": round(us, 3), "GB/s": round(b / us / 1e3, 1),
+                          "frac_hbm": round(b / us / 1e3 / hbm, 4)}), flush=True)
+        del x, q
+    for T in [1, 64, 1024, 8192]:
+        x = synth.rmsnorm_input(0, T, device=dev)
+        g = synth.rmsnorm_gamma(0, device=dev)
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        yq = torch.empty((T, H), dtype=torch.uint8, device=dev)
+        sf = mxq.empty_sf(1, T, H, dev)
+        us = timeit(lambda: mxq.rmsnorm_dual_out(x, g, synth.RMS_EPS, y, yq, sf_packed=sf))
+        b = rms_bytes(T)
+        print(json.dumps({"sweep": "rmsnorm_dual_out", "T": T, "us": round(us, 3), "GB/s": round(b / us / 1e3, 1),
+                          "frac_hbm": round(b / us / 1e3 / hbm, 4)}), flush=True)
+    for T in [1, 2, 4, 8, 16, 64, 128, 256, 384, 512, 1024, 2048, 4096, 8192, 16384, 32768]:
+        o = synth.o_proj_activation(0, T, device=dev)
+        oq, osf = mxq.quantize(o, layouts=(2,))
+        del o
+        O = mxq.MXFP8(oq, osf[2])
+        zq = torch.empty((T, KB), dtype=torch.uint8, device=dev)
+        zsf = mxq.empty_sf(2, T, KB, dev)
+        zb = torch.empty((T, KB), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((T, NB), dtype=torch.bfloat16, device=dev)
+        fused = timeit(lambda: mxq.o_proj_mxfp8(O, WA, WB, T, G, NA, KA, NB, zq, zsf, out))
+
+        def unfused():
+            mxq.wo_a_einsum_mxfp8(O, WA, T, G, NA, KA, z_bf16=zb)
+            mxq.mxfp8_quantize(zb, zq, None, None, zsf)
+            mxq.gemm_mxfp8_bf16(mxq.MXFP8(zq, zsf), WB, out)
+
+        unf = timeit(unfused)
+        wa_us = timeit(lambda: mxq.wo_a_einsum_mxfp8(O, WA, T, G, NA, KA, z_q=zq, z_sf_128x4=zsf))
+        wb_us = timeit(lambda: mxq.gemm_mxfp8_bf16(mxq.MXFP8(zq, zsf), WB, out))
+        byts = WEIGHT_BYTES + T * (G * KA * 33 // 32 + 2 * KB * 33 // 32 + NB * 2)
+        roof = max(byts / hbm / 1e3, FLOP_PER_TOKEN * T / mx_tf / 1e6)
+        print(json.dumps({"sweep": "o_proj", "T": T, "fused_us": round(fused, 3), "unfused_us": round(unf, 3),
+                          "saving_us": round(unf - fused, 3), "wo_a_us": round(wa_us, 3), "wo_b_us": round(wb_us, 3),
+                          "TFLOP/s": round(FLOP_PER_TOKEN * T / fused / 1e6, 1), "roofline_us": round(roof, 3),
+                          "frac": round(roof / fused, 4),
+                          "weight_GB/s": round(WEIGHT_BYTES / fused / 1e3, 1)}), flush=True)
+        del oq, osf, O, zq, zsf, zb, out
+
+
+# ---- the CPU oracle (cpu_baseline and the reference arm) -----------------------------------
+_ORACLE_STATE = {}
+
+
+def _oracle_setup(T_sample):
+    import numpy as np
+    import torch
+
+    import oracle
+    from mxfp8_activation_quant_gb300 import synth
+
+    if "wa_d" not in _ORACLE_STATE:
+        def bits(t):
+            return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+        waq, wasf = oracle.quantize_bf16(bits(synth.wo_a_weight(0)))
+        wbq, wbsf = oracle.quantize_bf16(bits(synth.wo_b_weight(0)))
+        _ORACLE_STATE["wa_d"] = oracle.dequant(waq, wasf)
+        _ORACLE_STATE["wb_d"] = oracle.dequant(wbq, wbsf)
+        _ORACLE_STATE["bits"] = bits
+    bits = _ORACLE_STATE["bits"]
+    rows = torch.arange(T_sample)
+    return (bits(synth.rmsnorm_input(0, T_sample)), bits(synth.rmsnorm_gamma(0)),
+            bits(synth.o_proj_activation(0, T_sample, rows=rows)))
+
+
+def _oracle_step(xb, gb, ob):
+    import oracle
+    from mxfp8_activation_quant_gb300 import synth
+
+    y = oracle.bf16_round(oracle.rmsnorm(xb, gb, synth.RMS_EPS))
+    oracle.quantize_bf16(y)
+    oq, osf = oracle.quantize_bf16(ob)
+    z = oracle.einsum_wo_a(oracle.dequant(oq, osf), _ORACLE_STATE["wa_d"], G)
+    zq, zsf = oracle.quantize_bf16(oracle.bf16_round(z))
+    return oracle.gemm_nt(oracle.dequant(zq, zsf), _ORACLE_STATE["wb_d"])
+
+
+def cpu_baseline(args, T, budget_s=15.0):
+    """The oracle as it stands, on the host cores, over a bounded token sample of the same
+    workload (RMSNorm + quantize + _o_proj for the first `n` tokens); tokens/s."""
+    import oracle
+
+    oracle.build()
+    n = 2
+    xb, gb, ob = _oracle_setup(n)
+    t0 = time.perf_counter()
+    _oracle_step(xb, gb, ob)
+    dt = time.perf_counter() - t0
+    n = max(2, min(T, int(n * budget_s / max(dt, 1e-3) / 2)))
+    xb, gb, ob = _oracle_setup(n)
+    t0 = time.perf_counter()
+    _oracle_step(xb, gb, ob)
+    dt = time.perf_counter() - t0
+    return {"value": round(n / dt, 3), "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"first {n} of the {T} tokens: fp64 RMSNorm + quantize + o quantize + wo_a + z quantize + wo_b"}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle timed on this machine's host cores, rank 0 only."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    import oracle
+
+    oracle.build()
+    T = args.tokens
+    n = max(1, args.ref_tokens)
+    xb, gb, ob = _oracle_setup(n)
+    for _ in range(args.warmup):
+        _oracle_step(xb, gb, ob)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(xb, gb, ob)
+    dt = time.perf_counter() - t0
+    tps = n * args.steps / dt
+    sample = f"{n} of the {T} tokens per step: fp64 RMSNorm + quantize + o quantize + wo_a + z quantize + wo_b"
+    res = {"impl": "reference", "metric": METRIC, "value": round(tps, 3), "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": {"workload": f"MXFP8 activation chain, DeepSeek-V4.1-Flash TP1 _o_proj + "
+                                                       f"RMSNorm, T={T}", "tokens": T},
+           "cpu_baseline": {"value": round(tps, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": round(tps, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--tokens", type=int, default=4096)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-tokens", type=int, default=4)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
