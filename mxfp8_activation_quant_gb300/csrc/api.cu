@@ -148,10 +148,18 @@ mxq_status wo_a_einsum_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, in
   return from_cuda(mxq::launch_gemm(l, static_cast<cudaStream_t>(stream)));
 }
 
-mxq_status gemm_mxfp8_bf16(const mxq_mx_tensor* a, const mxq_mx_tensor* b, int64_t M, int64_t N, int64_t K,
-                           void* out_bf16, int64_t ldo, void* status, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// wo_b launch shared by gemm_mxfp8_bf16 and o_proj_mxfp8. `pdl` makes it a programmatic
+// dependent of the previous kernel on the stream; only o_proj_mxfp8 sets it, because only
+// there is that kernel known (its own wo_a, which never writes the weights wo_b prefetches).
+mxq_status gemm_impl(const mxq_mx_tensor* a, const mxq_mx_tensor* b, int64_t M, int64_t N, int64_t K, void* out_bf16,
+                     int64_t ldo, void* status, void* stream, bool pdl) {
   if (M <= 0 || N <= 0 || K <= 0 || out_bf16 == nullptr) return MXQ_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % 128 != 0 || ldo < N) return MXQ_ERR_UNSUPPORTED_SHAPE;
+  if (N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return MXQ_ERR_UNSUPPORTED_SHAPE;
   mxq_status st = check_operand(a, M, K);
   if (st != MXQ_OK) return st;
   if ((st = check_operand(b, N, K)) != MXQ_OK) return st;
@@ -172,7 +180,17 @@ mxq_status gemm_mxfp8_bf16(const mxq_mx_tensor* a, const mxq_mx_tensor* b, int64
   l.out_bf16 = out_bf16;
   l.ldo = ldo;
   l.status = static_cast<int32_t*>(status);
+  l.pdl = pdl;
   return from_cuda(mxq::launch_gemm(l, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+mxq_status gemm_mxfp8_bf16(const mxq_mx_tensor* a, const mxq_mx_tensor* b, int64_t M, int64_t N, int64_t K,
+                           void* out_bf16, int64_t ldo, void* status, void* stream) {
+  return gemm_impl(a, b, M, N, K, out_bf16, ldo, status, stream, false);
 }
 
 mxq_status o_proj_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, const mxq_mx_tensor* wb, int64_t T,
@@ -188,7 +206,7 @@ mxq_status o_proj_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, const m
   st = wo_a_einsum_mxfp8(o, wa, T, G, Na, Ka, z_q, z_sf_128x4, z_sf_packed_i32, z_bf16, status, stream);
   if (st != MXQ_OK) return st;
   const mxq_mx_tensor z = {z_q, z_sf_128x4, MXQ_SF_TILED_128X4, T, Kb, Kb};
-  return gemm_mxfp8_bf16(&z, wb, T, Nb, Kb, out_bf16, Nb, status, stream);
+  return gemm_impl(&z, wb, T, Nb, Kb, out_bf16, Nb, status, stream, true);
 }
 
 }  // extern "C"

@@ -13,10 +13,13 @@
 // Two orientations:
 //   normal  (large T): A = activations (128 tokens / tile), B = weights (BN features / tile).
 //           TMEM lane = token row, so one thread holds a 32-column quantization group.
-//   swap-AB (T <= 256): A = weights (128 features / tile), B = activations (all tokens, BN).
-//           TMEM lane = feature, so a quantization group is one warp (32 lanes). The K range
-//           is split over a thread-block cluster; partial sums meet in distributed shared
-//           memory and are added in fixed rank order (deterministic, no atomics).
+//   swap-AB (T <= 512): A = weights (128 features / tile), B = activations (one token tile of
+//           N = 16..64, or 128-token tiles). TMEM lane = feature, so a quantization group is
+//           one warp (32 lanes). The K range is split over a thread-block cluster; partial sums
+//           meet in distributed shared memory and are added in fixed rank order
+//           (deterministic, no atomics).
+// Inside o_proj_mxfp8 the wo_b grid is a programmatic dependent of the wo_a grid: its CTAs
+// start while wo_a drains, fetch their first stages of weights, and only then wait for z.
 // Every mbarrier wait is bounded (about 1 s); a wait that gives up records MXQ_ERR_TIMEOUT in
 // the optional status word and the CTA drains its own copies and MMAs before leaving.
 #include <cuda.h>
@@ -35,12 +38,15 @@ constexpr int kThreads = 192;
 constexpr int BM = 128;            // MMA M: rows of the A operand = TMEM lanes
 constexpr int BK = 128;            // K bytes per stage = one 128-byte swizzle row
 constexpr int kStatusTimeout = 6;  // MXQ_ERR_TIMEOUT
+constexpr int kSwapMaxTokens = 512; // above this the normal orientation reuses operands better
 
 struct KArgs {
   int64_t T;
   int32_t n_feat;
   int32_t kb_per_cta;       // 128-wide k-blocks per CTA
   int32_t splits;           // swap-AB: CTAs per cluster along K
+  int32_t pdl;              // launched as a programmatic dependent: prefetch weights, then wait
+  int32_t per_rank_shift;   // log2(reduction columns owned by each cluster rank)
   int64_t act_k_per_group;  // activation column offset between groups
   const uint8_t* act_sf;
   int64_t act_gp4;  // 512-byte atoms per activation row tile
@@ -71,8 +77,15 @@ struct Cfg {
   static constexpr int TX_BYTES = A_BYTES + B_BYTES + SF_BYTES;
   static constexpr int OFF_B = STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
-  static constexpr int OFF_BAR = OFF_SF + STAGES * SF_BYTES;
-  static constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 1) * 8;
+  static constexpr int RC = BN < 128 ? BN : 128;  // split-K reduction columns per pass
+  // Token tiles of up to 64 columns reduce a K split through a dedicated receive buffer
+  // [source rank][feature][column] (fp32) filled by st.async; 128-column tiles reuse the
+  // (then idle) operand-tile region instead.
+  static constexpr bool RECV = BN <= 64;
+  static constexpr int RECV_BYTES = RECV ? RC * 128 * 4 : 0;
+  static constexpr int OFF_RECV = OFF_SF + STAGES * SF_BYTES;
+  static constexpr int OFF_BAR = OFF_RECV + RECV_BYTES;
+  static constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 2) * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr int TMEM_USED = BN + STAGES * SF_COLS;
   static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
@@ -87,10 +100,10 @@ struct Cfg {
   static constexpr int MAX_CO = 512 / TMEM_COLS;
   static constexpr int SMEM_FLOOR = SM_SMEM / (MAX_CO + 1) + 1024;
   static constexpr int SMEM_LAUNCH = SMEM_BYTES > SMEM_FLOOR ? SMEM_BYTES : SMEM_FLOOR;
-  static constexpr int RC = BN < 128 ? BN : 128;  // split-K reduction columns per pass
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
   static_assert(TMEM_USED <= 512, "TMEM");
-  static_assert(RC * 128 * 4 <= OFF_SF, "reduction buffer must fit in the tile region");
+  // reduction slots: 128 features x (RC + 4 * splits) floats, splits <= 8
+  static_assert(128 * (RC + 32) * 4 <= OFF_SF, "reduction buffer must fit in the tile region");
   static_assert(SMEM_LAUNCH <= 227 * 1024, "shared memory");
   static_assert(4 * (1 + SFB_ATOMS) <= SF_COLS, "scale slot");
 };
@@ -140,23 +153,45 @@ __device__ __forceinline__ void epi_row_chunk(const KArgs& p, const uint32_t (&a
   }
 }
 
-// swap orientation: one warp = 32 consecutive features (one quantization group), one token
-__device__ __forceinline__ void epi_feature_token(const KArgs& p, float v, int64_t t, int64_t col, int lane) {
-  const uint32_t hb = bf16x2_rn(v, 0.f) & 0xFFFFu;
+// scale byte 0 of a padding token row (t >= T) of the tiled / packed z scales
+__device__ __forceinline__ void epi_zero_scale(const KArgs& p, int64_t t, int64_t col) {
+  if (p.z_q == nullptr || t >= p.z_mp128) return;
+  const int64_t gi = col >> 5;
+  if (p.z_sf_tl != nullptr) p.z_sf_tl[tiled128x4_word_offset(t, gi >> 2, p.z_gp4) + (gi & 3)] = 0;
+  if (p.z_sf_pk != nullptr && t < p.z_mp4) p.z_sf_pk[((gi >> 2) * p.z_mp4 + t) * 4 + (gi & 3)] = 0;
+}
+
+// swap orientation, after the partial sums are in shared memory: one thread = one token and
+// one 32-feature quantization group. v[0..31] are the fp32 sums for features col..col+31 of
+// token t (col = first output column of the group).
+__device__ __forceinline__ void epi_token_group(const KArgs& p, const float (&v)[32], int64_t t, int64_t col) {
+  if (t >= p.z_mp128) return;
+  uint32_t hb[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) hb[i] = bf16x2_rn(v[2 * i], v[2 * i + 1]);
   const bool vt = t < p.T;
-  if (p.out_bf16 != nullptr && vt) p.out_bf16[t * p.ldo + col] = static_cast<uint16_t>(hb);
+  if (p.out_bf16 != nullptr && vt) {
+    uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + t * p.ldo + col);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hb[4 * i], hb[4 * i + 1], hb[4 * i + 2], hb[4 * i + 3]);
+  }
   if (p.z_q != nullptr) {
-    const uint32_t amax = __reduce_max_sync(0xffffffffu, hb & 0x7FFFu);
-    const uint32_t code = ue8m0_from_bf16_amax(amax);
-    const uint32_t byte = e4m3x2(bf16_lo(hb) * ue8m0_inverse(code), 0.f) & 0xFFu;
-    if (vt) p.z_q[t * p.ldz + col] = static_cast<uint8_t>(byte);
-    if (lane == 0) {
-      const int64_t gi = col >> 5;
-      if (p.z_sf_tl != nullptr)
-        p.z_sf_tl[tiled128x4_word_offset(t, gi >> 2, p.z_gp4) + (gi & 3)] = static_cast<uint8_t>(code);
-      if (p.z_sf_pk != nullptr && t < p.z_mp4)
-        p.z_sf_pk[((gi >> 2) * p.z_mp4 + t) * 4 + (gi & 3)] = static_cast<uint8_t>(code);
+    const uint32_t code = ue8m0_from_bf16_amax(amax_bf16x2_words(hb, 16));
+    const float s = ue8m0_inverse(code);
+    uint32_t qw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      qw[i] = e4m3x2(bf16_lo(hb[2 * i]) * s, bf16_hi(hb[2 * i]) * s) |
+              (e4m3x2(bf16_lo(hb[2 * i + 1]) * s, bf16_hi(hb[2 * i + 1]) * s) << 16);
+    if (vt) {
+      uint4* dst = reinterpret_cast<uint4*>(p.z_q + t * p.ldz + col);
+      dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+      dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
     }
+    const int64_t gi = col >> 5;
+    if (p.z_sf_tl != nullptr) p.z_sf_tl[tiled128x4_word_offset(t, gi >> 2, p.z_gp4) + (gi & 3)] = static_cast<uint8_t>(code);
+    if (p.z_sf_pk != nullptr && t < p.z_mp4)
+      p.z_sf_pk[((gi >> 2) * p.z_mp4 + t) * 4 + (gi & 3)] = static_cast<uint8_t>(code);
   }
 }
 
@@ -172,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_full = sbase + C::OFF_BAR;      // STAGES x 8 B
   const uint32_t bar_empty = bar_full + STAGES * 8;  // STAGES x 8 B
   const uint32_t bar_accf = bar_empty + STAGES * 8;  // 8 B
+  const uint32_t bar_recv = bar_accf + 8;            // 8 B: split-K partials received
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   int* issued_cnt = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
@@ -190,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     split = blockIdx.z % p.splits;
     m0 = static_cast<int64_t>(blockIdx.x) * BM;
     a_row0 = static_cast<int64_t>(g) * p.n_feat + m0;  // weights
-    b_row0 = 0;                                        // activations
+    b_row0 = static_cast<int64_t>(blockIdx.y) * BN;    // activations (token tile)
     a_xoff = 0;
     b_xoff = static_cast<int64_t>(g) * p.act_k_per_group;
     a_sf = p.wt_sf;
@@ -199,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     a_kc0 = 0;
     b_sf = p.act_sf;
     b_gp4 = p.act_gp4;
-    b_rt0 = 0;
+    b_rt0 = b_row0 >> 7;  // BN == 128 whenever there is more than one token tile
     b_kc0 = b_xoff >> 7;
   } else {
     g = blockIdx.z;
@@ -230,6 +266,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_accf, 1);
+    if (SWAP && C::RECV && p.splits > 1) {
+      mbar_init(bar_recv, 1);
+      // every rank (this one included) sends 128 features x per_rank columns of fp32
+      mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>(p.splits * 128 * (C::RC / p.splits) * 4));
+    }
     *abort_flag = 0;
     *issued_cnt = 0;
     *consumed_cnt = 0;
@@ -243,10 +284,53 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // peers may push into this CTA's receive buffer only after its barrier is initialized:
+  // arrive now, wait just before the first push (by then every peer has long arrived)
+  const bool recv_path = SWAP && C::RECV && p.splits > 1;
+  if (recv_path) cluster_arrive();
+  // A dependent grid (wo_b after wo_a) may start its prologue once every CTA of this grid has
+  // passed this point: at once for the single-wave swap-AB grids, at the epilogue otherwise.
+  if (SWAP && threadIdx.x == 0) pdl_launch_dependents();
 
   // ---- roles ----
   if (warp == 0 && lane == 0) {
+    const uint32_t a_dst0 = sbase, b_dst0 = sbase + C::OFF_B, sf_dst0 = sbase + C::OFF_SF;
+    // operand loads of k-block i into stage s; the weight operand is A in swap-AB, B otherwise
+    auto load_act = [&](int s, int kb, uint32_t fb) {
+      if (SWAP) {
+        tma_load_2d(b_dst0 + s * C::B_BYTES, &tm_b, fb, static_cast<int32_t>(b_xoff + kb * BK), static_cast<int32_t>(b_row0));
+#pragma unroll
+        for (int j = 0; j < C::SFB_ATOMS; ++j)
+          bulk_load(sf_dst0 + s * C::SF_BYTES + 512 * (1 + j), b_sf + ((b_rt0 + j) * b_gp4 + b_kc0 + kb) * 512, 512, fb);
+      } else {
+        tma_load_2d(a_dst0 + s * C::A_BYTES, &tm_a, fb, static_cast<int32_t>(a_xoff + kb * BK), static_cast<int32_t>(a_row0));
+        bulk_load(sf_dst0 + s * C::SF_BYTES, a_sf + (a_rt * a_gp4 + a_kc0 + kb) * 512, 512, fb);
+      }
+    };
+    auto load_wt = [&](int s, int kb, uint32_t fb) {
+      if (SWAP) {
+        tma_load_2d(a_dst0 + s * C::A_BYTES, &tm_a, fb, static_cast<int32_t>(a_xoff + kb * BK), static_cast<int32_t>(a_row0));
+        bulk_load(sf_dst0 + s * C::SF_BYTES, a_sf + (a_rt * a_gp4 + a_kc0 + kb) * 512, 512, fb);
+      } else {
+        tma_load_2d(b_dst0 + s * C::B_BYTES, &tm_b, fb, static_cast<int32_t>(b_xoff + kb * BK), static_cast<int32_t>(b_row0));
+#pragma unroll
+        for (int j = 0; j < C::SFB_ATOMS; ++j)
+          bulk_load(sf_dst0 + s * C::SF_BYTES + 512 * (1 + j), b_sf + ((b_rt0 + j) * b_gp4 + b_kc0 + kb) * 512, 512, fb);
+      }
+    };
     int i = 0;
+    if (p.pdl) {
+      // the first STAGES stages are free: fetch their weights while the producer of the
+      // activations may still be running, then wait for it and fetch the activations
+      const int pre = nk < STAGES ? nk : STAGES;
+      for (int j = 0; j < pre; ++j) {
+        mbar_arrive_expect_tx(bar_full + 8 * j, C::TX_BYTES);
+        load_wt(j, kb_begin + j, bar_full + 8 * j);
+      }
+      pdl_wait_primary();
+      for (int j = 0; j < pre; ++j) load_act(j, kb_begin + j, bar_full + 8 * j);
+      i = pre;
+    }
     for (; i < nk; ++i) {
       const int s = i % STAGES;
       const uint32_t ph = (i / STAGES) & 1;
@@ -259,15 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kb = kb_begin + i;
       const uint32_t fb = bar_full + 8 * s;
       mbar_arrive_expect_tx(fb, C::TX_BYTES);
-      tma_load_2d(sbase + s * C::A_BYTES, &tm_a, fb, static_cast<int32_t>(a_xoff + kb * BK),
-                  static_cast<int32_t>(a_row0));
-      tma_load_2d(sbase + C::OFF_B + s * C::B_BYTES, &tm_b, fb, static_cast<int32_t>(b_xoff + kb * BK),
-                  static_cast<int32_t>(b_row0));
-      const uint32_t sf_dst = sbase + C::OFF_SF + s * C::SF_BYTES;
-      bulk_load(sf_dst, a_sf + (a_rt * a_gp4 + a_kc0 + kb) * 512, 512, fb);
-#pragma unroll
-      for (int j = 0; j < C::SFB_ATOMS; ++j)
-        bulk_load(sf_dst + 512 * (1 + j), b_sf + ((b_rt0 + j) * b_gp4 + b_kc0 + kb) * 512, 512, fb);
+      load_wt(s, kb, fb);
+      load_act(s, kb, fb);
     }
     *issued_cnt = i;
   } else if (warp == 1 && lane == 0) {
@@ -313,6 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (!SWAP) {
+    if (threadIdx.x == 64) pdl_launch_dependents();
     if (epi && !__any_sync(0xffffffffu, *abort_flag)) {
       const int64_t row = m0 + 32 * q + lane;
       const int64_t col0 = static_cast<int64_t>(g) * p.n_feat + static_cast<int64_t>(blockIdx.x) * BN;
@@ -325,57 +403,123 @@ __global__ void __launch_bounds__(kThreads, 1)
         epi_row_chunk(p, acc, row, col0 + 32 * c, word, c);
       }
     }
-  } else if (p.splits == 1) {
+  } else if (recv_path) {
+    // K split over the cluster, token tile <= 64 columns. Each rank st.async's its fp32 partial
+    // of the columns owned by rank o (columns [o*per_rank, (o+1)*per_rank)) into rank o's
+    // receive buffer, slot [source rank][feature][column]; the bytes complete on rank o's
+    // mbarrier. Each owner then adds its slots in rank order 0..splits-1 (deterministic) and
+    // finishes whole (token, 32-feature group) items.
+    const uint32_t rank = cluster_ctarank();
+    const int per_rank = C::RC / p.splits;
+    const int f = 32 * q + lane;
+    const uint32_t recv = sbase + C::OFF_RECV;
+    cluster_wait();
     if (epi && !__any_sync(0xffffffffu, *abort_flag)) {
-      const int64_t col = static_cast<int64_t>(g) * p.n_feat + m0 + 32 * q + lane;
 #pragma unroll 1
-      for (int c = 0; c < BN / 16; ++c) {
+      for (int c = 0; c < C::RC / 16; ++c) {
         uint32_t acc[16];
         tmem_ld_x16(t_lane + 16 * c, acc);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) epi_feature_token(p, __uint_as_float(acc[j]), 16 * c + j, col, lane);
+        for (int k = 0; k < 4; ++k) {
+          const int cc = 16 * c + 4 * k;  // first of 4 columns, all owned by one rank
+          const uint32_t owner = static_cast<uint32_t>(cc >> p.per_rank_shift);
+          const int li = cc & (per_rank - 1);
+          const uint32_t off = recv + static_cast<uint32_t>(((static_cast<int>(rank) * 128 + f) * per_rank + li) * 4);
+          st_async_v4(mapa_shared(off, owner), acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3],
+                      mapa_shared(bar_recv, owner));
+        }
+      }
+    }
+    if (epi) {
+      if (!mbar_wait_bounded(bar_recv, 0)) {
+        *abort_flag = 1;
+        report_timeout(p.status);
+      }
+      if (!__any_sync(0xffffffffu, *abort_flag)) {
+        const float* red = reinterpret_cast<const float*>(smem + C::OFF_RECV);
+        const int items = per_rank * 4;
+        for (int w = static_cast<int>(threadIdx.x) - 64; w < items; w += 128) {
+          const int j = w & (per_rank - 1);
+          const int gq = w >> p.per_rank_shift;
+          const int64_t t = b_row0 + static_cast<int>(rank) * per_rank + j;
+          const int64_t col = static_cast<int64_t>(g) * p.n_feat + m0 + 32 * gq;
+          if (t >= p.T) {  // padding token: only its zero scale is stored
+            epi_zero_scale(p, t, col);
+            continue;
+          }
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = red[(32 * gq + i) * per_rank + j];
+          for (int r = 1; r < p.splits; ++r) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += red[((r * 128) + 32 * gq + i) * per_rank + j];
+          }
+          epi_token_group(p, v, t, col);
+        }
       }
     }
   } else {
-    // split-K over the cluster: partials -> own smem [col][128 features] fp32, then rank r sums
-    // its share of the columns from every rank's buffer in rank order.
-    const uint32_t rank = cluster_ctarank();
+    // Partial sums go to shared memory as slots [source rank][feature][token] (rows padded by
+    // 4 floats: conflict-free 16-byte writes and 4-byte reads). With a K split over the
+    // cluster, every rank writes the columns (tokens) owned by rank c / per_rank into that
+    // rank's slots, once all ranks' pipelines are idle; after the second barrier each owner
+    // adds its slots in rank order 0..splits-1 (deterministic) for its tokens. Then every
+    // thread finishes whole (token, 32-feature group) items: no shuffles, 16-byte stores.
+    const bool split = p.splits > 1;
+    const uint32_t rank = split ? cluster_ctarank() : 0u;
     const int per_rank = C::RC / p.splits;
-    const int64_t col = static_cast<int64_t>(g) * p.n_feat + m0 + 32 * q + lane;
-    const uint32_t red = sbase;  // reuses the tile region: all copies and MMAs are complete
+    const int ps = per_rank + 4;  // padded slot row, in floats
+    const int f = 32 * q + lane;
+    const float* red = reinterpret_cast<const float*>(smem);  // reuses the tile region
 #pragma unroll 1
     for (int pass = 0; pass < BN / C::RC; ++pass) {
+      if (split) cluster_sync_all();  // all ranks' tile regions are free / owners done reading
+      else if (pass > 0 && epi) named_barrier(1, 128);
       if (epi && !__any_sync(0xffffffffu, *abort_flag)) {
 #pragma unroll 1
         for (int c = 0; c < C::RC / 16; ++c) {
           uint32_t acc[16];
           tmem_ld_x16(t_lane + pass * C::RC + 16 * c, acc);
           tmem_ld_wait();
-          float* dst = reinterpret_cast<float*>(smem) + (16 * c) * 128 + 32 * q + lane;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) dst[j * 128] = __uint_as_float(acc[j]);
+          for (int k = 0; k < 4; ++k) {
+            const int cc = 16 * c + 4 * k;  // first of 4 tokens, all owned by one rank
+            const uint32_t owner = static_cast<uint32_t>(cc >> p.per_rank_shift);
+            const int li = cc & (per_rank - 1);
+            const uint32_t off = sbase + static_cast<uint32_t>(((static_cast<int>(rank) * 128 + f) * ps + li) * 4);
+            if (split)
+              st_dsmem_v4(mapa_shared(off, owner), acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+            else
+              st_smem_v4(off, acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+          }
         }
       }
-      cluster_sync_all();
+      if (split) cluster_sync_all();
+      else if (epi) named_barrier(1, 128);
       if (epi && !__any_sync(0xffffffffu, *abort_flag)) {
-#pragma unroll 1
-        for (int j = 0; j < per_rank; ++j) {
-          const int tl = static_cast<int>(rank) * per_rank + j;  // column inside this pass
-          const uint32_t off = red + static_cast<uint32_t>((tl * 128 + 32 * q + lane) * 4);
-          float v = ld_dsmem_f32(mapa_shared(off, 0));
-          for (int r = 1; r < p.splits; ++r) v += ld_dsmem_f32(mapa_shared(off, static_cast<uint32_t>(r)));
-          epi_feature_token(p, v, pass * C::RC + tl, col, lane);
+        const int items = per_rank * 4;  // (token, group) pairs owned by this rank
+        for (int w = static_cast<int>(threadIdx.x) - 64; w < items; w += 128) {
+          const int j = w & (per_rank - 1);
+          const int gq = w >> p.per_rank_shift;
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = red[(32 * gq + i) * ps + j];
+          for (int r = 1; r < p.splits; ++r) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += red[((r * 128) + 32 * gq + i) * ps + j];
+          }
+          const int64_t t = b_row0 + pass * C::RC + static_cast<int>(rank) * per_rank + j;
+          epi_token_group(p, v, t, static_cast<int64_t>(g) * p.n_feat + m0 + 32 * gq);
         }
       }
-      cluster_sync_all();
     }
   }
 
   // swap orientation: tiled z scales of padding token rows [BN, ceil(T/128)*128) are zero
-  if (SWAP && epi && p.z_sf_tl != nullptr && split == 0) {
+  if (SWAP && epi && p.z_sf_tl != nullptr && split == 0 && blockIdx.y == gridDim.y - 1) {
     const int64_t wi = (static_cast<int64_t>(g) * p.n_feat + m0) >> 7;
-    for (int64_t t = BN + (static_cast<int>(threadIdx.x) - 64); t < p.z_mp128; t += 128)
+    for (int64_t t = b_row0 + BN + (static_cast<int>(threadIdx.x) - 64); t < p.z_mp128; t += 128)
       *reinterpret_cast<uint32_t*>(p.z_sf_tl + tiled128x4_word_offset(t, wi, p.z_gp4)) = 0u;
   }
 
@@ -388,6 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         (void)mbar_wait_bounded(bar_full + 8 * (i % STAGES), (i / STAGES) & 1);
     }
     if (warp == 1 && lane == 0) (void)mbar_wait_bounded(bar_accf, 0);
+    if (recv_path && warp == 0 && lane == 0) (void)mbar_wait_bounded(bar_recv, 0);
     __syncthreads();
   }
   if (warp == 1) {
@@ -458,14 +603,19 @@ cudaError_t launch_cfg(const GemmLaunch& l, const KArgs& ka, dim3 grid, int clus
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_LAUNCH;
   cfg.stream = stream;
-  cudaLaunchAttribute attrs[1];
+  cudaLaunchAttribute attrs[2];
   cfg.numAttrs = 0;
   if (cluster_z > 1) {
-    attrs[0].id = cudaLaunchAttributeClusterDimension;
-    attrs[0].val.clusterDim.x = 1;
-    attrs[0].val.clusterDim.y = 1;
-    attrs[0].val.clusterDim.z = static_cast<unsigned>(cluster_z);
-    cfg.numAttrs = 1;
+    attrs[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+    attrs[cfg.numAttrs].val.clusterDim.x = 1;
+    attrs[cfg.numAttrs].val.clusterDim.y = 1;
+    attrs[cfg.numAttrs].val.clusterDim.z = static_cast<unsigned>(cluster_z);
+    ++cfg.numAttrs;
+  }
+  if (ka.pdl) {
+    attrs[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    ++cfg.numAttrs;
   }
   cfg.attrs = attrs;
   if (SWAP) return cudaLaunchKernelEx(&cfg, kern, tma_wt, tma_act, ka);
@@ -476,19 +626,22 @@ cudaError_t launch_cfg(const GemmLaunch& l, const KArgs& ka, dim3 grid, int clus
 // columns and keeps every CTA resident in one wave.
 int pick_splits(int tiles, int kb_total, int rc, int slots) {
   for (int s = 8; s > 1; s >>= 1)
-    if (kb_total % s == 0 && rc % s == 0 && tiles * s <= slots) return s;
+    if (kb_total % s == 0 && rc / s >= 4 && tiles * s <= slots) return s;
   return 1;
 }
 
 template <int BN, int STAGES>
 cudaError_t launch_swap(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
-  const int tiles = l.G * (l.n_feat / BM);
+  const int tok_tiles = static_cast<int>(ceil_div(l.T, BN));
+  const int tiles = l.G * (l.n_feat / BM) * tok_tiles;
   const int kb_total = l.k_len / BK;
   const int slots = num_sms() * ctas_per_sm<BN, STAGES>();
   const int s = pick_splits(tiles, kb_total, Cfg<BN, STAGES>::RC, slots);
   ka.splits = s;
   ka.kb_per_cta = kb_total / s;
-  dim3 grid(static_cast<unsigned>(l.n_feat / BM), 1, static_cast<unsigned>(l.G * s));
+  ka.per_rank_shift = 0;
+  while ((1 << ka.per_rank_shift) < Cfg<BN, STAGES>::RC / s) ++ka.per_rank_shift;
+  dim3 grid(static_cast<unsigned>(l.n_feat / BM), static_cast<unsigned>(tok_tiles), static_cast<unsigned>(l.G * s));
   return launch_cfg<BN, STAGES, true>(l, ka, grid, s, stream);
 }
 
@@ -522,12 +675,14 @@ cudaError_t launch_gemm(const GemmLaunch& l, cudaStream_t stream) {
   ka.z_sf_pk = static_cast<uint8_t*>(l.z_sf_packed);
   ka.z_mp4 = ceil_div(l.T, 4) * 4;
   ka.status = l.status;
+  ka.pdl = l.pdl ? 1 : 0;
   if (l.n_feat % BM != 0 || l.k_len % BK != 0) return cudaErrorInvalidValue;
+  // swap-AB (weights on the MMA's M side) while the token count is small: one token tile of
+  // N = 16..128, or several 128-token tiles
   if (l.T <= 16) return launch_swap<16, 5>(l, ka, stream);
   if (l.T <= 32) return launch_swap<32, 4>(l, ka, stream);
-  if (l.T <= 64) return launch_swap<64, 4>(l, ka, stream);
-  if (l.T <= 128) return launch_swap<128, 3>(l, ka, stream);
-  if (l.T <= 256) return launch_swap<256, 2>(l, ka, stream);
+  if (l.T <= 64) return launch_swap<64, 3>(l, ka, stream);
+  if (l.T <= kSwapMaxTokens) return launch_swap<128, 3>(l, ka, stream);
   if (l.n_feat % 256 == 0) return launch_normal<256, 4>(l, ka, stream);
   return launch_normal<128, 6>(l, ka, stream);
 }

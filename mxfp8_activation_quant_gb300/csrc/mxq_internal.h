@@ -51,6 +51,9 @@ struct GemmLaunch {
   void* z_sf_tiled;         // F8_128x4 scales of z (needs z_q)
   void* z_sf_packed;        // int32-packed MN-major scales of z (needs z_q)
   int32_t* status;          // optional device status word
+  // Launch as a programmatic dependent of the previous kernel on the stream: the weight
+  // operand (never written by that kernel) is prefetched before waiting for it to finish.
+  bool pdl;
 };
 cudaError_t launch_gemm(const GemmLaunch& a, cudaStream_t stream);
 
