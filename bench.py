@@ -314,27 +314,46 @@ TRAFFIC = {}
 
 def sweep(args, mxq, synth, torch, dev, WA, WB):
     """Per-config lines for the sweep tables (not the headline line): quantizer, RMSNorm, and
-    the _o_proj pair fused vs unfused (wo_a bf16 z -> standalone quantize -> wo_b)."""
+    the _o_proj pair fused vs unfused (wo_a bf16 z -> standalone quantize -> wo_b), timed under
+    CUDA-graph replay with a cold L2 (the pages' method: "full CUDA graph, cold L2")."""
     hbm, bf16_tf, _ = load_peaks()
     mx_tf = 2 * bf16_tf
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(4 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    cap = torch.cuda.Stream(dev)
+
     def timeit(fn, reps=20):
-        ts = []
-        for i in range(3):
-            flush.fill_(i)
+        """us per call, the way the pages time _o_proj: the calls replayed from a CUDA graph with
+        an L2 flush before each, minus the same graph holding only the flushes."""
+        with torch.cuda.stream(cap):
             fn()
-        for i in range(reps):
-            flush.fill_(i)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            b.synchronize()
-            ts.append(a.elapsed_time(b) * 1e3)
-        return statistics.median(ts)
+            flush.fill_(0)
+        torch.cuda.synchronize()
+        g1, g0 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g1, stream=cap):
+            for i in range(reps):
+                flush.fill_(i & 0xFF)
+                fn()
+        with torch.cuda.graph(g0, stream=cap):
+            for i in range(reps):
+                flush.fill_(i & 0xFF)
+        per = []
+        for g in (g1, g0):
+            g.replay()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                g.replay()
+                b.record()
+                b.synchronize()
+                ts.append(a.elapsed_time(b) * 1e3 / reps)
+            per.append(statistics.median(ts))
+        del g1, g0
+        return per[0] - per[1]
 
     for T in [1, 16, 256, 4096, 32768]:
         x = synth.quantizer_input(0, T, device=dev)

@@ -110,9 +110,13 @@ mxq_status rmsnorm_dual_out(const void* x_bf16, const void* gamma_bf16, float ep
   return from_cuda(mxq::launch_rmsnorm(l, static_cast<cudaStream_t>(stream)));
 }
 
-mxq_status wo_a_einsum_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, int64_t T, int32_t G, int32_t Na,
-                             int32_t Ka, void* z_q, void* z_sf_128x4, void* z_sf_packed_i32, void* z_bf16,
-                             void* status, void* stream) {
+}  // extern "C"
+
+namespace {
+
+mxq_status wo_a_impl(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, int64_t T, int32_t G, int32_t Na, int32_t Ka,
+                     void* z_q, void* z_sf_128x4, void* z_sf_packed_i32, void* z_bf16, void* status, void* stream,
+                     bool has_dependent) {
   if (T <= 0 || G <= 0 || Na <= 0 || Ka <= 0) return MXQ_ERR_INVALID_ARG;
   if ((z_q == nullptr) != (z_sf_128x4 == nullptr)) return MXQ_ERR_INVALID_ARG;
   if (z_q == nullptr && z_bf16 == nullptr) return MXQ_ERR_INVALID_ARG;
@@ -145,7 +149,18 @@ mxq_status wo_a_einsum_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, in
   l.z_sf_tiled = z_sf_128x4;
   l.z_sf_packed = z_sf_packed_i32;
   l.status = static_cast<int32_t*>(status);
+  l.has_dependent = has_dependent;
   return from_cuda(mxq::launch_gemm(l, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+mxq_status wo_a_einsum_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, int64_t T, int32_t G, int32_t Na,
+                             int32_t Ka, void* z_q, void* z_sf_128x4, void* z_sf_packed_i32, void* z_bf16,
+                             void* status, void* stream) {
+  return wo_a_impl(o, wa, T, G, Na, Ka, z_q, z_sf_128x4, z_sf_packed_i32, z_bf16, status, stream, false);
 }
 
 }  // extern "C"
@@ -203,7 +218,7 @@ mxq_status o_proj_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, const m
   mxq_status st = check_operand(wb, Nb, Kb);
   if (st != MXQ_OK) return st;
   if (!al16(out_bf16)) return MXQ_ERR_MISALIGNED;
-  st = wo_a_einsum_mxfp8(o, wa, T, G, Na, Ka, z_q, z_sf_128x4, z_sf_packed_i32, z_bf16, status, stream);
+  st = wo_a_impl(o, wa, T, G, Na, Ka, z_q, z_sf_128x4, z_sf_packed_i32, z_bf16, status, stream, true);
   if (st != MXQ_OK) return st;
   const mxq_mx_tensor z = {z_q, z_sf_128x4, MXQ_SF_TILED_128X4, T, Kb, Kb};
   return gemm_impl(&z, wb, T, Nb, Kb, out_bf16, Nb, status, stream, true);

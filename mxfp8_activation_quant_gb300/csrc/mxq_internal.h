@@ -54,6 +54,9 @@ struct GemmLaunch {
   // Launch as a programmatic dependent of the previous kernel on the stream: the weight
   // operand (never written by that kernel) is prefetched before waiting for it to finish.
   bool pdl;
+  // A programmatic dependent grid follows this one (wo_a inside o_proj_mxfp8): prefer a
+  // lighter per-CTA footprint so that the dependent's CTAs can be resident alongside.
+  bool has_dependent;
 };
 cudaError_t launch_gemm(const GemmLaunch& a, cudaStream_t stream);
 
