@@ -17,6 +17,7 @@ alongside. `--impl reference` times the CPU oracle on a bounded sample of the sa
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -278,7 +279,7 @@ def run_gpu(args):
         roof = {"kernel": names[dom], "bound": "hbm", "achieved": round(byts[dom] / dom_us / 1e3, 1),
                 "peak": hbm, "unit": "GB/s", "peak_note": f"{peak_kind} copy bandwidth"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = TRAFFIC.get((names[dom], T))
+    roof["traffic"] = traffic_for(names[dom], T)
 
     clocks = sampler.summary()
     res = {
@@ -307,9 +308,22 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-# per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from the committed ncu
-# captures, keyed by (kernel, tokens); None until a capture of the current kernel exists
-TRAFFIC = {}
+# Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from the committed ncu
+# captures (profiles/), keyed by (kernel, tokens), with the sources the capture was taken on and
+# their SHA-1: once those sources change the figure no longer describes the kernel and reads null.
+_GEMM_SRC = ("mxfp8_activation_quant_gb300/csrc/gemm_mxf8.cu", "mxfp8_activation_quant_gb300/csrc/mxq_device.cuh")
+TRAFFIC = {
+    ("wo_b_mxfp8", 4096): (92_935_168 + 24_913_664, _GEMM_SRC, "0ee2d57b55b99025"),
+}
+
+
+def traffic_for(kernel, T):
+    entry = TRAFFIC.get((kernel, T))
+    if entry is None:
+        return None
+    nbytes, srcs, sha = entry
+    blob = b"".join(open(os.path.join(ROOT, f), "rb").read() for f in srcs)
+    return nbytes if hashlib.sha1(blob).hexdigest()[:16] == sha else None
 
 
 def sweep(args, mxq, synth, torch, dev, WA, WB):
