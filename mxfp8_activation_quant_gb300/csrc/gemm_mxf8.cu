@@ -78,12 +78,15 @@ struct Cfg {
   static constexpr int TX_BYTES = A_BYTES + B_BYTES + SF_BYTES;
   static constexpr int OFF_B = STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
-  static constexpr int RC = BN < 128 ? BN : 128;  // split-K reduction columns per pass
-  // Token tiles of up to 64 columns reduce a K split through a dedicated receive buffer
-  // [source rank][feature][column] (fp32) filled by st.async; 128-column tiles reuse the
-  // (then idle) operand-tile region instead.
-  static constexpr bool RECV = BN <= 64;
-  static constexpr int RECV_BYTES = RECV ? RC * 128 * 4 : 0;
+  // Split-K reduction (swap-AB). Token tiles of 16 columns (decode) push their partials
+  // with per-thread st.async into a dedicated receive buffer [source rank][feature][column] as
+  // soon as their own MMAs are done (PUSH). Wider tiles stage their partials in the operand
+  // tiles once their MMAs have completed (BN * 512 bytes, one block per owner) and receive the
+  // peers' blocks there too ((splits - 1) / splits of that), after a cluster barrier that every
+  // CTA reaches after its MMAs; split_fits() bounds the split accordingly.
+  static constexpr bool PUSH = BN <= 16;
+  static constexpr int RECV_BYTES = PUSH ? 128 * BN * 4 : 0;
+  static constexpr bool split_fits(int s) { return PUSH || BN * 512 + BN * 512 / s * (s - 1) <= OFF_SF; }
   static constexpr int OFF_RECV = OFF_SF + STAGES * SF_BYTES;
   static constexpr int OFF_BAR = OFF_RECV + RECV_BYTES;
   static constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 4) * 8;  // full, empty, 4 more
@@ -103,13 +106,20 @@ struct Cfg {
   static constexpr int SMEM_LAUNCH = SMEM_BYTES > SMEM_FLOOR ? SMEM_BYTES : SMEM_FLOOR;
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
   static_assert(TMEM_USED <= 512, "TMEM");
-  // reduction slots: 128 features x (RC + 4 * splits) floats, splits <= 8
-  static_assert(128 * (RC + 32) * 4 <= OFF_SF, "reduction buffer must fit in the tile region");
+  // unsplit swap-AB epilogue: 128 features x (BN + 4) floats staged in the tile region
+  static_assert(128 * (BN + 4) * 4 <= OFF_SF, "epilogue staging must fit in the tile region");
   static_assert(SMEM_LAUNCH <= 227 * 1024, "shared memory");
   static_assert(4 * (1 + SFB_ATOMS) <= SF_COLS, "scale slot");
 };
 
 // ---- epilogue helpers ----------------------------------------------------------------------
+// Split-K staging blocks: row `row` of a block holds `cpr` 16-byte chunks; chunk c is stored at
+// c ^ recv_swizzle(row, cpr), which spreads 8 consecutive rows over the 8 chunk positions of a
+// 128-byte bank line (fewer when a row has fewer than 8 chunks).
+__device__ __forceinline__ int recv_swizzle(int row, int cpr) {
+  return cpr >= 8 ? (row & 7) : ((row * cpr) >> 3) & (cpr - 1);
+}
+
 __device__ __forceinline__ uint32_t amax_bf16x2_words(const uint32_t* hb, int n) {
   uint32_t m = 0;
 #pragma unroll
@@ -197,7 +207,7 @@ __device__ __forceinline__ void epi_token_group(const KArgs& p, const float (&v)
 }
 
 template <int BN, int STAGES, bool SWAP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 3)
     gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                      const KArgs p) {
   using C = Cfg<BN, STAGES>;
@@ -267,10 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_accf, 1);
-    if (SWAP && C::RECV && p.splits > 1) {
+    if (SWAP && p.splits > 1) {
       mbar_init(bar_recv, 1);
-      // every rank (this one included) sends 128 features x per_rank columns of fp32
-      mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>(p.splits * 128 * (C::RC / p.splits) * 4));
+      // PUSH: every rank, this one included, sends 128 features x (BN / splits) columns of fp32;
+      // otherwise each other rank sends one block of that size
+      mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>(C::PUSH ? 128 * BN * 4 : 128 * BN * 4 / p.splits * (p.splits - 1)));
     }
     *abort_flag = 0;
     *issued_cnt = 0;
@@ -285,10 +296,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // peers may push into this CTA's receive buffer only after its barrier is initialized:
-  // arrive now, wait just before the first push (by then every peer has long arrived)
-  const bool recv_path = SWAP && C::RECV && p.splits > 1;
-  if (recv_path) cluster_arrive();
+  const bool recv_path = SWAP && p.splits > 1;
+  // PUSH: peers may write this CTA's receive buffer once its barrier is initialized; arrive now,
+  // wait just before the first push (by then every peer has long arrived)
+  if (C::PUSH && recv_path) cluster_arrive();
   // A dependent grid (wo_b after wo_a) may start its prologue once every CTA of this grid has
   // passed this point: at once for the single-wave swap-AB grids, at the epilogue otherwise.
   if (SWAP && threadIdx.x == 0) pdl_launch_dependents();
@@ -404,20 +415,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         epi_row_chunk(p, acc, row, col0 + 32 * c, word, c);
       }
     }
-  } else if (recv_path) {
-    // K split over the cluster, token tile <= 64 columns. Each rank st.async's its fp32 partial
-    // of the columns owned by rank o (columns [o*per_rank, (o+1)*per_rank)) into rank o's
-    // receive buffer, slot [source rank][feature][column]; the bytes complete on rank o's
-    // mbarrier. Each owner then adds its slots in rank order 0..splits-1 (deterministic) and
+  } else if (C::PUSH && recv_path) {
+    // K split over the cluster, token tile of 16 columns. Each rank st.async's its fp32
+    // partial of the columns owned by rank o (columns [o*per_rank, (o+1)*per_rank)) into rank
+    // o's receive buffer, slot [source rank][feature][column]; the bytes complete on rank o's
+    // mbarrier. Each owner adds its slots in rank order 0..splits-1 (deterministic) and
     // finishes whole (token, 32-feature group) items.
     const uint32_t rank = cluster_ctarank();
-    const int per_rank = C::RC / p.splits;
+    const int per_rank = BN / p.splits;
     const int f = 32 * q + lane;
     const uint32_t recv = sbase + C::OFF_RECV;
     cluster_wait();
     if (epi && !__any_sync(0xffffffffu, *abort_flag)) {
 #pragma unroll 1
-      for (int c = 0; c < C::RC / 16; ++c) {
+      for (int c = 0; c < BN / 16; ++c) {
         uint32_t acc[16];
         tmem_ld_x16(t_lane + 16 * c, acc);
         tmem_ld_wait();
@@ -460,59 +471,119 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else {
-    // Partial sums go to shared memory as slots [source rank][feature][token] (rows padded by
-    // 4 floats: conflict-free 16-byte writes and 4-byte reads). With a K split over the
-    // cluster, every rank writes the columns (tokens) owned by rank c / per_rank into that
-    // rank's slots, once all ranks' pipelines are idle; after the second barrier each owner
-    // adds its slots in rank order 0..splits-1 (deterministic) for its tokens. Then every
-    // thread finishes whole (token, 32-feature group) items: no shuffles, 16-byte stores.
-    const bool split = p.splits > 1;
-    const uint32_t rank = split ? cluster_ctarank() : 0u;
-    const int per_rank = C::RC / p.splits;
-    const int ps = per_rank + 4;  // padded slot row, in floats
+  } else if (recv_path) {
+    // K split over the cluster; rank o owns the token columns [o*per_rank, (o+1)*per_rank).
+    // Every rank stages its fp32 partial in its own shared memory, one block per owner laid out
+    // [feature][column] with the 16-byte chunks of each feature row XOR-swizzled (conflict-free
+    // 16-byte writes by 8 lanes, conflict-free column reads by a warp). It then sends each other
+    // owner its block with one bulk shared-to-shared copy, counted on the owner's mbarrier: a
+    // handful of large transfers, where per-thread remote stores would each update that
+    // mbarrier. Each owner adds the blocks of ranks 0..splits-1 in rank order (deterministic)
+    // and finishes whole (token, 32-feature group) items.
+    const uint32_t rank = cluster_ctarank();
+    const int per_rank = BN / p.splits;
+    const uint32_t blk = static_cast<uint32_t>(128 * per_rank * 4);
+    const uint32_t stage0 = sbase;              // p.splits blocks: this rank's partial
+    const uint32_t recv0 = sbase + BN * 512;    // p.splits - 1 blocks: the peers' partials
+    const int cpr = per_rank >> 2;              // 16-byte chunks per feature row
     const int f = 32 * q + lane;
-    const float* red = reinterpret_cast<const float*>(smem);  // reuses the tile region
+    if (epi && !__any_sync(0xffffffffu, *abort_flag)) {
+      const int sw = recv_swizzle(f, cpr);
 #pragma unroll 1
-    for (int pass = 0; pass < BN / C::RC; ++pass) {
-      if (split) cluster_sync_all();  // all ranks' tile regions are free / owners done reading
-      else if (pass > 0 && epi) named_barrier(1, 128);
-      if (epi && !__any_sync(0xffffffffu, *abort_flag)) {
-#pragma unroll 1
-        for (int c = 0; c < C::RC / 16; ++c) {
-          uint32_t acc[16];
-          tmem_ld_x16(t_lane + pass * C::RC + 16 * c, acc);
-          tmem_ld_wait();
+      for (int c = 0; c < BN / 16; ++c) {
+        uint32_t acc[16];
+        tmem_ld_x16(t_lane + 16 * c, acc);
+        tmem_ld_wait();
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int cc = 16 * c + 4 * k;  // first of 4 tokens, all owned by one rank
-            const uint32_t owner = static_cast<uint32_t>(cc >> p.per_rank_shift);
-            const int li = cc & (per_rank - 1);
-            const uint32_t off = sbase + static_cast<uint32_t>(((static_cast<int>(rank) * 128 + f) * ps + li) * 4);
-            if (split)
-              st_dsmem_v4(mapa_shared(off, owner), acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
-            else
-              st_smem_v4(off, acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
-          }
+        for (int k = 0; k < 4; ++k) {
+          const int cc = 16 * c + 4 * k;  // first of 4 columns, all owned by one rank
+          const uint32_t owner = static_cast<uint32_t>(cc >> p.per_rank_shift);
+          const int chunk = ((cc & (per_rank - 1)) >> 2) ^ sw;
+          st_smem_v4(stage0 + owner * blk + static_cast<uint32_t>((f * per_rank + 4 * chunk) * 4), acc[4 * k],
+                     acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
         }
       }
-      if (split) cluster_sync_all();
-      else if (epi) named_barrier(1, 128);
-      if (epi && !__any_sync(0xffffffffu, *abort_flag)) {
-        const int items = per_rank * 4;  // (token, group) pairs owned by this rank
-        for (int w = static_cast<int>(threadIdx.x) - 64; w < items; w += 128) {
-          const int j = w & (per_rank - 1);
-          const int gq = w >> p.per_rank_shift;
-          float v[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = red[(32 * gq + i) * ps + j];
-          for (int r = 1; r < p.splits; ++r) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] += red[((r * 128) + 32 * gq + i) * ps + j];
-          }
-          const int64_t t = b_row0 + pass * C::RC + static_cast<int>(rank) * per_rank + j;
-          epi_token_group(p, v, t, static_cast<int64_t>(g) * p.n_feat + m0 + 32 * gq);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    // every CTA of the cluster has finished its MMAs (epilogue warps arrive after bar_accf) and
+    // staged its blocks: the operand regions that hold the receive blocks are idle
+    cluster_arrive();
+    cluster_wait();
+    if (threadIdx.x == 64 && !*abort_flag) {
+      for (int d = 1; d < p.splits; ++d) {
+        const uint32_t o = (rank + d) % p.splits;
+        const uint32_t slot = (rank + p.splits - o - 1) % p.splits;  // this rank among o's sources
+        bulk_s2s(mapa_shared(recv0 + slot * blk, o), stage0 + o * blk, blk, mapa_shared(bar_recv, o));
+      }
+    }
+    if (epi) {
+      if (!mbar_wait_bounded(bar_recv, 0)) {
+        *abort_flag = 1;
+        report_timeout(p.status);
+      }
+    }
+    // arrives once every copy into this CTA has landed (its senders may leave after the matching
+    // wait in the teardown)
+    __syncwarp();
+    cluster_arrive();
+    if (epi && !__any_sync(0xffffffffu, *abort_flag)) {
+      const float* sm = reinterpret_cast<const float*>(smem);
+      const int items = per_rank * 4;
+      for (int w = static_cast<int>(threadIdx.x) - 64; w < items; w += 128) {
+        const int j = w & (per_rank - 1);
+        const int gq = w >> p.per_rank_shift;
+        const int64_t t = b_row0 + static_cast<int>(rank) * per_rank + j;
+        const int64_t col = static_cast<int64_t>(g) * p.n_feat + m0 + 32 * gq;
+        if (t >= p.T) {  // padding token: only its zero scale is stored
+          epi_zero_scale(p, t, col);
+          continue;
         }
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        for (int r = 0; r < p.splits; ++r) {
+          const uint32_t rr = static_cast<uint32_t>(r);
+          const uint32_t base = rr == rank ? stage0 + rank * blk : recv0 + ((rr + p.splits - rank - 1) % p.splits) * blk;
+          const float* blkp = sm + (base - sbase) / 4;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int row = 32 * gq + i;
+            const float x = blkp[row * per_rank + 4 * ((j >> 2) ^ recv_swizzle(row, cpr)) + (j & 3)];
+            v[i] = r == 0 ? x : v[i] + x;
+          }
+        }
+        epi_token_group(p, v, t, col);
+      }
+    }
+  } else {
+    // Unsplit K: the accumulator goes to shared memory as [feature][token] (rows padded by 4
+    // floats: conflict-free 16-byte writes and 4-byte reads); then every thread finishes whole
+    // (token, 32-feature group) items: no shuffles, 16-byte stores.
+    constexpr int ps = BN + 4;
+    const int f = 32 * q + lane;
+    const float* red = reinterpret_cast<const float*>(smem);  // reuses the tile region
+    if (epi && !__any_sync(0xffffffffu, *abort_flag)) {
+#pragma unroll 1
+      for (int c = 0; c < BN / 16; ++c) {
+        uint32_t acc[16];
+        tmem_ld_x16(t_lane + 16 * c, acc);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          st_smem_v4(sbase + static_cast<uint32_t>((f * ps + 16 * c + 4 * k) * 4), acc[4 * k], acc[4 * k + 1],
+                     acc[4 * k + 2], acc[4 * k + 3]);
+      }
+    }
+    if (epi) named_barrier(1, 128);
+    if (epi && !__any_sync(0xffffffffu, *abort_flag)) {
+      for (int w = static_cast<int>(threadIdx.x) - 64; w < BN * 4; w += 128) {
+        const int j = w & (BN - 1);
+        const int gq = w / BN;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = red[(32 * gq + i) * ps + j];
+        epi_token_group(p, v, b_row0 + j, static_cast<int64_t>(g) * p.n_feat + m0 + 32 * gq);
       }
     }
   }
@@ -533,9 +604,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         (void)mbar_wait_bounded(bar_full + 8 * (i % STAGES), (i / STAGES) & 1);
     }
     if (warp == 1 && lane == 0) (void)mbar_wait_bounded(bar_accf, 0);
-    if (recv_path && warp == 0 && lane == 0) (void)mbar_wait_bounded(bar_recv, 0);
     __syncthreads();
   }
+  // bulk path: every copy in the cluster has landed, so no peer still reads this CTA's blocks
+  if (recv_path && !C::PUSH) cluster_wait();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -781,6 +853,14 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int6
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Dynamic shared memory limit. The L1/shared split stays the driver's choice: forcing the
+// largest carveout lets a programmatic dependent's CTAs (wo_b) sit beside wo_a's, where their
+// early weight loads slow wo_a more than they save (measured on the T <= 16 pair).
+template <typename K>
+cudaError_t set_smem_attrs(K kern, int bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
 int num_sms() {
   int dev = 0, n = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
@@ -801,8 +881,7 @@ template <int BN, int STAGES, bool SWAP>
 cudaError_t launch_cfg(const GemmLaunch& l, const KArgs& ka, dim3 grid, int cluster_z, cudaStream_t stream) {
   using C = Cfg<BN, STAGES>;
   auto kern = gemm_mxf8_kernel<BN, STAGES, SWAP>;
-  static const cudaError_t attr_err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_LAUNCH);
+  static const cudaError_t attr_err = set_smem_attrs(kern, C::SMEM_LAUNCH);
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap tma_act, tma_wt;
   if (!make_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, SWAP ? BN : BM)) return cudaErrorInvalidValue;
@@ -832,11 +911,13 @@ cudaError_t launch_cfg(const GemmLaunch& l, const KArgs& ka, dim3 grid, int clus
   return cudaLaunchKernelEx(&cfg, kern, tma_act, tma_wt, ka);
 }
 
-// Largest split of the K range (cluster size) that divides the k-blocks and the reduction
-// columns and keeps every CTA resident in one wave.
-int pick_splits(int tiles, int kb_total, int rc, int slots) {
+// Largest split of the K range (cluster size) that divides the k-blocks, leaves every rank at
+// least 4 token columns, fits its staging in shared memory and keeps every CTA resident in one
+// wave.
+template <int BN, int STAGES>
+int pick_splits(int tiles, int kb_total, int slots) {
   for (int s = 8; s > 1; s >>= 1)
-    if (kb_total % s == 0 && rc / s >= 4 && tiles * s <= slots) return s;
+    if (kb_total % s == 0 && BN / s >= 4 && Cfg<BN, STAGES>::split_fits(s) && tiles * s <= slots) return s;
   return 1;
 }
 
@@ -846,11 +927,11 @@ cudaError_t launch_swap(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   const int tiles = l.G * (l.n_feat / BM) * tok_tiles;
   const int kb_total = l.k_len / BK;
   const int slots = num_sms() * ctas_per_sm<BN, STAGES>();
-  const int s = pick_splits(tiles, kb_total, Cfg<BN, STAGES>::RC, slots);
+  const int s = pick_splits<BN, STAGES>(tiles, kb_total, slots);
   ka.splits = s;
   ka.kb_per_cta = kb_total / s;
   ka.per_rank_shift = 0;
-  while ((1 << ka.per_rank_shift) < Cfg<BN, STAGES>::RC / s) ++ka.per_rank_shift;
+  while ((1 << ka.per_rank_shift) < BN / s) ++ka.per_rank_shift;
   dim3 grid(static_cast<unsigned>(l.n_feat / BM), static_cast<unsigned>(tok_tiles), static_cast<unsigned>(l.G * s));
   return launch_cfg<BN, STAGES, true>(l, ka, grid, s, stream);
 }
@@ -869,8 +950,7 @@ template <int BN, int STAGES>
 cudaError_t launch_persistent(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   using C = Cfg<BN, STAGES>;
   auto kern = gemm_mxf8_persistent<BN, STAGES>;
-  static const cudaError_t attr_err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_LAUNCH);
+  static const cudaError_t attr_err = set_smem_attrs(kern, C::SMEM_LAUNCH);
   if (attr_err != cudaSuccess) return attr_err;
   ka.splits = 1;
   ka.kb_per_cta = l.k_len / BK;
@@ -921,12 +1001,14 @@ cudaError_t launch_gemm(const GemmLaunch& l, cudaStream_t stream) {
   if (l.n_feat % BM != 0 || l.k_len % BK != 0) return cudaErrorInvalidValue;
   // swap-AB (weights on the MMA's M side) while the token count is small: one token tile of
   // N = 16..128, or several 128-token tiles
-  // T <= 16: a grid followed by a dependent (wo_a of o_proj_mxfp8) uses 3 stages (67 KB of
-  // shared memory) so the dependent wo_b CTAs fit beside it and prefetch their weights; a
-  // stand-alone grid keeps 5 stages so that about 14 MB of loads are in flight
+  // T <= 16: a grid followed by a dependent (wo_a of o_proj_mxfp8) uses 3 stages so that the
+  // dependent wo_b CTAs that find room start early and fetch their first weight stages; other
+  // grids keep 5 stages, about 14 MB of loads in flight
   if (l.T <= 16) return l.has_dependent ? launch_swap<16, 3>(l, ka, stream) : launch_swap<16, 5>(l, ka, stream);
-  if (l.T <= 32) return launch_swap<32, 4>(l, ka, stream);
-  if (l.T <= 64) return launch_swap<64, 3>(l, ka, stream);
+  if (l.T <= 32) return launch_swap<32, 5>(l, ka, stream);
+  if (l.T <= 64) return launch_swap<64, 4>(l, ka, stream);
+  if (l.T <= 128) return launch_swap<128, 6>(l, ka, stream);
+  if (l.T <= 256) return launch_swap<128, 3>(l, ka, stream);
   if (l.T <= kSwapMaxTokens) return launch_swap<128, 3>(l, ka, stream);
   if (l.n_feat % 256 == 0) return launch_persistent<256, 4>(l, ka, stream);
   return launch_normal<128, 6>(l, ka, stream);

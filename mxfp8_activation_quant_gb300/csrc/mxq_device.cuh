@@ -266,6 +266,19 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t a, ui
                "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
                : "memory");
 }
+// Bulk copy from this CTA's shared memory into a cluster peer's (addresses from mapa); the
+// bytes complete on the peer's mbarrier `remote_bar`. 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_s2s(uint32_t remote_dst, uint32_t src, uint32_t bytes, uint32_t remote_bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   remote_dst),
+               "r"(src), "r"(bytes), "r"(remote_bar)
+               : "memory");
+}
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy reads
+// (bulk copies) of them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
