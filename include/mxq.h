@@ -186,6 +186,33 @@ MXQ_API mxq_status o_proj_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa,
                                 void* z_sf_128x4, void* z_sf_packed_i32, void* z_bf16, void* out_bf16,
                                 void* status, void* stream);
 
+/*
+ * o_proj_mxfp8_noalloc -- o_proj_mxfp8 with the z hand-off held in a fixed buffer inside the
+ * library, so the caller passes no z buffers and nothing is allocated. The pages have no
+ * counterpart: they always hand z over in a caller-owned tensor.
+ *
+ * For callers that cannot or will not allocate device memory per call: a plain C host with
+ * no caching allocator (cudaMalloc / cudaFree synchronize the device, which would stall a
+ * decode loop), or a runtime that fixes its device memory at start-up.
+ *
+ * Arguments as in o_proj_mxfp8 without z_q / z_sf_128x4 / z_sf_packed_i32 / z_bf16. The
+ * buffer holds at most MXQ_NOALLOC_Z_BYTES of E4M3 z (T * G * Na bytes) and
+ * MXQ_NOALLOC_SF_BYTES of F8_128x4 scales (mxq_sf_bytes(MXQ_SF_TILED_128X4, T, G * Na)); that is
+ * T <= 256 for the DeepSeek-V4.1 shapes (G * Na = 8192). Larger shapes return
+ * MXQ_ERR_UNSUPPORTED_SHAPE before anything is launched.
+ *
+ * Nothing in the buffer needs to start at zero: wo_a writes every z byte and scale that wo_b
+ * reads in the same call. The first call on a device looks the buffer up
+ * (cudaGetSymbolAddress, checked: MXQ_ERR_CUDA on failure); make that first call outside any
+ * stream capture. All calls on one device share the one buffer: calls that overlap in time
+ * (different streams or threads) race on it, so order them on one stream.
+ */
+#define MXQ_NOALLOC_Z_BYTES (2u << 20)
+#define MXQ_NOALLOC_SF_BYTES (64u << 10)
+MXQ_API mxq_status o_proj_mxfp8_noalloc(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, const mxq_mx_tensor* wb,
+                                        int64_t T, int32_t G, int32_t Na, int32_t Ka, int32_t Nb, void* out_bf16,
+                                        void* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -58,7 +58,12 @@ SIGNATURES = {
     "wo_a_einsum_mxfp8": ([_MXP, _MXP, I64, I32, I32, I32, P, P, P, P, P, P], ctypes.c_int),
     "gemm_mxfp8_bf16": ([_MXP, _MXP, I64, I64, I64, P, I64, P, P], ctypes.c_int),
     "o_proj_mxfp8": ([_MXP, _MXP, _MXP, I64, I32, I32, I32, I32, P, P, P, P, P, P, P], ctypes.c_int),
+    "o_proj_mxfp8_noalloc": ([_MXP, _MXP, _MXP, I64, I32, I32, I32, I32, P, P, P], ctypes.c_int),
 }
+
+# capacity of the library-held z buffer of o_proj_mxfp8_noalloc (include/mxq.h)
+NOALLOC_Z_BYTES = 2 << 20
+NOALLOC_SF_BYTES = 64 << 10
 
 
 def load():
@@ -191,3 +196,11 @@ def o_proj_mxfp8(o: MXFP8, wa: MXFP8, wb: MXFP8, T: int, G: int, Na: int, Ka: in
     _check(load().o_proj_mxfp8(ctypes.byref(oc), ctypes.byref(ac), ctypes.byref(bc), T, G, Na, Ka, Nb, _ptr(z_q),
                                _ptr(z_sf_128x4), _ptr(z_sf_packed), _ptr(z_bf16), _ptr(out), _ptr(status),
                                _stream(stream)), "o_proj_mxfp8")
+
+
+def o_proj_mxfp8_noalloc(o: MXFP8, wa: MXFP8, wb: MXFP8, T: int, G: int, Na: int, Ka: int, Nb: int,
+                         out: torch.Tensor, status=None, stream=None) -> None:
+    """o_proj_mxfp8 with z held in the library's fixed buffer (no z arguments, nothing allocated)."""
+    oc, ac, bc = o.c(), wa.c(), wb.c()
+    _check(load().o_proj_mxfp8_noalloc(ctypes.byref(oc), ctypes.byref(ac), ctypes.byref(bc), T, G, Na, Ka, Nb,
+                                       _ptr(out), _ptr(status), _stream(stream)), "o_proj_mxfp8_noalloc")

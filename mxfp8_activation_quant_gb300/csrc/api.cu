@@ -9,18 +9,22 @@
 #include "mxq_internal.h"
 
 namespace {
-
 thread_local char g_last_error[128] = "no error";
+}  // namespace
 
-inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
-mxq_status from_cuda(cudaError_t e) {
+mxq_status mxq::from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return MXQ_OK;
   std::strncpy(g_last_error, cudaGetErrorName(e), sizeof(g_last_error) - 1);
   g_last_error[sizeof(g_last_error) - 1] = '\0';
   return MXQ_ERR_CUDA;
 }
+
+namespace {
+
+using mxq::from_cuda;
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // An MXFP8 GEMM operand: [rows, cols] E4M3 with F8_128x4 scales.
 mxq_status check_operand(const mxq_mx_tensor* t, int64_t rows, int64_t cols) {

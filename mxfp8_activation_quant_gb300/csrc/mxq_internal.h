@@ -5,7 +5,12 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "mxq.h"
+
 namespace mxq {
+
+// CUDA error -> MXQ_OK / MXQ_ERR_CUDA; records the error name for mxq_last_error_string.
+mxq_status from_cuda(cudaError_t e);
 
 struct QuantizeLaunch {
   const void* x;

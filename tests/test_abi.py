@@ -27,7 +27,7 @@ def test_every_declared_symbol_is_exported(lib):
     from mxfp8_activation_quant_gb300 import _lib
 
     names = declared_functions()
-    assert len(names) == 11, names
+    assert len(names) == 12, names
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(_lib.SIGNATURES)
@@ -99,3 +99,20 @@ def test_gemm_argument_errors(lib):
     assert p(B(o), B(wa), B(wb), 8, 8, 1024, 4096, 5120, None, FAKE, None, None, FAKE, None, None) == 1
     assert p(B(o), B(wa), B(mx(5120, 8192, layout=1)), 8, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE,
              None, None) == 4
+
+
+def test_o_proj_noalloc_argument_errors(lib):
+    from mxfp8_activation_quant_gb300._lib import NOALLOC_Z_BYTES, MxTensorC
+
+    def mx(rows, cols):
+        return MxTensorC(FAKE, FAKE, 2, rows, cols, cols)
+
+    B = ctypes.byref
+    n = lib.o_proj_mxfp8_noalloc
+    t_max = NOALLOC_Z_BYTES // 8192  # 256 tokens for G * Na = 8192
+    # shapes beyond the fixed buffer are refused before any CUDA call
+    for T in (t_max + 1, 4096):
+        assert n(B(mx(T, 32768)), B(mx(8192, 4096)), B(mx(5120, 8192)), T, 8, 1024, 4096, 5120, FAKE, None,
+                 None) == 2
+    assert n(B(mx(0, 32768)), B(mx(8192, 4096)), B(mx(5120, 8192)), 0, 8, 1024, 4096, 5120, FAKE, None, None) == 1
+    assert n(B(mx(4, 32768)), B(mx(8192, 4096)), B(mx(5120, 8192)), 4, 8, 1000, 4096, 5120, FAKE, None, None) == 2
