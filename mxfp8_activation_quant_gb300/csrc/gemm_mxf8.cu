@@ -824,6 +824,281 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 }
 
 // ------------------------------------------------------------------------------------------
+// CTA-pair persistent kernel (large T). One tcgen05 MMA of M = 256 tokens x N = 256 features
+// spans the two CTAs of a cluster (cta_group::2). Each CTA streams its own 128 token rows and
+// 128 of the 256 weight rows: 32 KB of operands per 128-deep k-block and CTA, against 48 KB for
+// a 128 x 256 tile on one SM, for the same tensor work per SM. Both CTAs' loads complete on the
+// even CTA's stage barriers; the even CTA's MMA warp issues the MMAs, and their commits arrive
+// on both CTAs' barriers. Each CTA drains its half of the accumulator (its 128 token rows x 256
+// columns, in its own TMEM) exactly as gemm_mxf8_persistent does.
+// ------------------------------------------------------------------------------------------
+template <int STAGES>
+struct PairCfg {
+  static constexpr int A_BYTES = BM * BK;   // this CTA's 128 token rows
+  static constexpr int B_BYTES = 128 * BK;  // this CTA's 128 of the 256 weight rows
+  static constexpr int SF_BYTES = 512 * 3;  // scale atoms: A (own rows), B (both 128-row atoms)
+  static constexpr int TX_BYTES = 2 * (A_BYTES + B_BYTES + SF_BYTES);  // both CTAs, even CTA's barrier
+  static constexpr int OFF_B = STAGES * A_BYTES;
+  static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_BAR = OFF_SF + STAGES * SF_BYTES;
+  static constexpr int OFF_MISC = OFF_BAR + (3 * STAGES + 4) * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int SF_COLS = 16;
+  static constexpr int TMEM_COLS = 512;  // 256 accumulator columns + STAGES x 16 scale columns
+  static_assert(256 + STAGES * SF_COLS <= TMEM_COLS, "TMEM");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+constexpr int kThreadsPair = 352;  // warp 0 TMA, 1 MMA, 2..9 epilogue, 10 scale copies
+
+template <int STAGES>
+__global__ void __launch_bounds__(kThreadsPair, 1)
+    gemm_mxf8_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                   const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
+                   const KArgs p) {
+  using C = PairCfg<STAGES>;
+  constexpr int BN = 256;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t sraw = smem_u32(smem_raw);
+  const uint32_t sbase = (sraw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - sraw);
+  const uint32_t bar_full = sbase + C::OFF_BAR;      // stage full (both CTAs' bytes), even CTA only
+  const uint32_t bar_empty = bar_full + STAGES * 8;  // stage empty, arrived by the MMA commits
+  const uint32_t bar_accf = bar_empty + STAGES * 8;  // accumulator full (MMA -> both epilogues)
+  const uint32_t bar_acce = bar_accf + 8;            // accumulator empty (16 epilogue warps), even CTA
+  const uint32_t bar_drain = bar_accf + 16;          // abort path: all tcgen05 ops completed
+  const uint32_t bar_sf = bar_accf + 24;             // STAGES x 8 B: scale atoms of a stage in TMEM
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  int* issued_cnt = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
+  int* consumed_cnt = reinterpret_cast<int*>(smem + C::OFF_MISC + 12);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0 issues the MMAs
+  const bool leader = rank == 0;
+
+  const int n_tiles = p.n_feat / BN;
+  const int m_pairs = static_cast<int>((p.T + 2 * BM - 1) / (2 * BM));
+  const int per_group = m_pairs * n_tiles;
+  const int total = per_group * p.G;
+  const int nk = p.kb_per_cta;
+  const int first_tile = static_cast<int>(blockIdx.x >> 1), tile_step = static_cast<int>(gridDim.x >> 1);
+  // pair tile -> (group, first token of the 256-token pair tile, first feature)
+  auto decode = [&](int t, int& g, int64_t& m0, int64_t& n0) {
+    g = t / per_group;
+    const int r = t - g * per_group;
+    m0 = static_cast<int64_t>(r / n_tiles) * (2 * BM);
+    n0 = static_cast<int64_t>(r % n_tiles) * BN;
+  };
+
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_b);
+    tma_prefetch_desc(&tm_sfa);
+    tma_prefetch_desc(&tm_sfb);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_accf, 1);
+    mbar_init(bar_acce, 16);  // one arrival per epilogue warp of both CTAs
+    mbar_init(bar_drain, 2);  // the MMA thread and the scale-copy thread
+    for (int s = 0; s < STAGES; ++s) mbar_init(bar_sf + 8 * s, 1);
+    *abort_flag = 0;
+    *issued_cnt = 0;
+    *consumed_cnt = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before any load or commit can reach them
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- producer (both CTAs) ----------------
+    const uint32_t full0 = mapa_shared(bar_full, 0);  // the even CTA's stage barriers
+    int it = 0;
+    bool first = true;
+    for (int t = first_tile; t < total && !*abort_flag; t += tile_step) {
+      int g;
+      int64_t m0, n0;
+      decode(t, g, m0, n0);
+      const int64_t a_row = m0 + BM * rank;  // this CTA's token rows
+      const int64_t a_x = static_cast<int64_t>(g) * p.act_k_per_group;
+      const int64_t a_atom = (a_row >> 7) * p.act_gp4 + (a_x >> 7);  // scale atom of k-block 0
+      const int64_t b_first = static_cast<int64_t>(g) * p.n_feat + n0;
+      const int64_t b_row = b_first + 128 * rank;  // this CTA's weight rows
+      const int64_t b_atom = (b_first >> 7) * p.wt_gp4;
+      auto load_act = [&](int s, int kb, uint32_t fb) {
+        tma_load_2d_pair(sbase + s * C::A_BYTES, &tm_a, fb, static_cast<int32_t>(a_x + kb * BK), static_cast<int32_t>(a_row));
+        tma_load_2d_pair(sbase + C::OFF_SF + s * C::SF_BYTES, &tm_sfa, fb, 0, static_cast<int32_t>(a_atom + kb));
+      };
+      auto load_wt = [&](int s, int kb, uint32_t fb) {
+        const uint32_t sf = sbase + C::OFF_SF + s * C::SF_BYTES;
+        tma_load_2d_pair(sbase + C::OFF_B + s * C::B_BYTES, &tm_b, fb, static_cast<int32_t>(kb * BK), static_cast<int32_t>(b_row));
+        tma_load_2d_pair(sf + 512, &tm_sfb, fb, 0, static_cast<int32_t>(b_atom + kb));
+        tma_load_2d_pair(sf + 1024, &tm_sfb, fb, 0, static_cast<int32_t>(b_atom + p.wt_gp4 + kb));
+      };
+      int kb = 0;
+      if (first && p.pdl) {
+        const int pre = nk < STAGES ? nk : STAGES;
+        for (int j = 0; j < pre; ++j) {
+          if (leader) mbar_arrive_expect_tx(bar_full + 8 * j, C::TX_BYTES);
+          load_wt(j, j, full0 + 8 * j);
+        }
+        pdl_wait_primary();
+        for (int j = 0; j < pre; ++j) load_act(j, j, full0 + 8 * j);
+        kb = pre;
+        it = pre;
+      }
+      first = false;
+      for (; kb < nk; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!mbar_wait_bounded(bar_empty + 8 * s, ph ^ 1)) {
+          *abort_flag = 1;
+          report_timeout(p.status);
+          break;
+        }
+        if (leader) mbar_arrive_expect_tx(bar_full + 8 * s, C::TX_BYTES);
+        load_wt(s, kb, full0 + 8 * s);
+        load_act(s, kb, full0 + 8 * s);
+      }
+    }
+    *issued_cnt = it;
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer (even CTA) ----------------
+    if (leader) {
+      // The MMAs of a stage wait for its scale atoms in TMEM (bar_sf), which warp 10 copies as
+      // soon as the stage's operands have landed: the copies are issued by another thread, so
+      // this thread's MMA stream never waits behind a copy of its own.
+      int it = 0, ti = 0;
+      for (int t = first_tile; t < total && !*abort_flag; t += tile_step, ++ti) {
+        if (!mbar_wait_bounded(bar_acce, (ti & 1) ^ 1)) {  // both halves drained by the epilogues
+          *abort_flag = 1;
+          report_timeout(p.status);
+          break;
+        }
+        tc_fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait_bounded(bar_sf + 8 * s, (it / STAGES) & 1)) {
+            *abort_flag = 1;
+            report_timeout(p.status);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa_t = tmem + BN + s * C::SF_COLS;
+          const uint32_t sfb_t = sfa_t + 4;
+          const uint64_t ad = sdesc_kmajor_sw128(sbase + s * C::A_BYTES);
+          const uint64_t bd = sdesc_kmajor_sw128(sbase + C::OFF_B + s * C::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k)
+            tc_mma_mxf8_pair(tmem, ad + 2 * k, bd + 2 * k, idesc_mxf8(2 * BM, BN, k, k), sfa_t, sfb_t,
+                             (kb | k) != 0 ? 1u : 0u);
+          tc_commit_pair(bar_empty + 8 * s, 0x3);
+        }
+        tc_commit_pair(bar_accf, 0x3);
+        if (!ok) break;
+      }
+      *consumed_cnt = it;
+    }
+    pdl_launch_dependents();  // every tile of this pair has been issued
+  } else if (warp == 10) {
+    // ---------------- scale copies (even CTA) ----------------
+    if (leader && lane == 0) {
+      const int my_tiles = first_tile < total ? (total - 1 - first_tile) / tile_step + 1 : 0;
+      const int n_iter = my_tiles * nk;
+      for (int it = 0; it < n_iter && !*abort_flag; ++it) {
+        const int s = it % STAGES;
+        if (!mbar_wait_bounded(bar_full + 8 * s, (it / STAGES) & 1)) {
+          *abort_flag = 1;
+          report_timeout(p.status);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sf_src = sbase + C::OFF_SF + s * C::SF_BYTES;
+        const uint32_t sfa_t = tmem + BN + s * C::SF_COLS;
+        tc_cp_sf_atom_pair(sfa_t, sdesc_sf_atom(sf_src));
+        tc_cp_sf_atom_pair(sfa_t + 4, sdesc_sf_atom(sf_src + 512));
+        tc_cp_sf_atom_pair(sfa_t + 8, sdesc_sf_atom(sf_src + 1024));
+        tc_commit_pair(bar_sf + 8 * s, 0x1);
+      }
+    }
+  } else if (warp >= 2) {
+    // ---------------- epilogue (both CTAs) ----------------
+    const int q = warp & 3;            // TMEM lane quarter
+    const int half = (warp - 2) >> 2;  // accumulator columns [128*half, 128*half + 128)
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16) + 128 * half;
+    const uint32_t acce0 = mapa_shared(bar_acce, 0);
+    int ti = 0;
+    for (int t = first_tile; t < total; t += tile_step, ++ti) {
+      if (!mbar_wait_bounded(bar_accf, ti & 1)) {
+        *abort_flag = 1;
+        report_timeout(p.status);
+      }
+      if (__any_sync(0xffffffffu, *abort_flag)) break;
+      tc_fence_after();
+      uint32_t acc[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_x32(t_lane + 32 * c, acc[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {  // the MMA warp may overwrite this half of the accumulator now
+        if (leader)
+          mbar_arrive(bar_acce);
+        else
+          mbar_arrive_remote(acce0);
+      }
+      int g;
+      int64_t m0, n0;
+      decode(t, g, m0, n0);
+      const int64_t row0 = m0 + BM * rank;
+      if (row0 >= p.z_mp128) continue;  // this half of a ragged last pair tile holds no token
+      const int64_t row = row0 + 32 * q + lane;
+      const int64_t col0 = static_cast<int64_t>(g) * p.n_feat + n0 + 128 * half;
+      uint32_t word = 0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) epi_row_chunk(p, acc[c], row, col0 + 32 * c, word, c);
+    }
+  }
+  __syncwarp();
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs have left their loops: issue counts and abort flags are final
+  if (leader && warp == 0 && lane == 0) {
+    const int peer_abort = ld_dsmem_s32(mapa_shared(smem_u32(const_cast<int*>(abort_flag)), 1));
+    if (*abort_flag || peer_abort) {
+      // wait (bounded) for every stage either CTA issued and the MMA warp did not consume
+      const int peer_issued = ld_dsmem_s32(mapa_shared(smem_u32(issued_cnt), 1));
+      const int hi = *issued_cnt > peer_issued ? *issued_cnt : peer_issued;
+      for (int i = *consumed_cnt; i < hi; ++i)
+        (void)mbar_wait_bounded(bar_full + 8 * (i % STAGES), (i / STAGES) & 1);
+      *abort_flag = 1;
+    }
+  }
+  __syncthreads();
+  if (leader && (warp == 1 || warp == 10) && lane == 0 && *abort_flag) {
+    tc_commit_pair(bar_drain, 0x1);  // arrives once every MMA / copy this thread issued has completed
+    if (warp == 1) (void)mbar_wait_bounded(bar_drain, 0);
+  }
+  __syncthreads();
+  cluster_sync_all();  // the pair's MMAs and copies are over before either CTA frees TMEM or leaves
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -859,6 +1134,19 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int6
 template <typename K>
 cudaError_t set_smem_attrs(K kern, int bytes) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+// Scale atoms of an F8_128x4 array as a 2-D tensor [atoms, 128 x u32]: one 512-byte atom per box.
+bool make_sf_map(CUtensorMap* m, const void* base, int64_t atoms) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {128u, static_cast<cuuint64_t>(atoms)};
+  cuuint64_t strides[1] = {512u};
+  cuuint32_t box[2] = {128u, 1u};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int num_sms() {
@@ -977,6 +1265,44 @@ cudaError_t launch_persistent(const GemmLaunch& l, KArgs ka, cudaStream_t stream
 
 }  // namespace
 
+// CTA-pair persistent launch: clusters of two, one CTA per SM, pair tiles of 256 x 256
+template <int STAGES>
+cudaError_t launch_pair(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
+  using C = PairCfg<STAGES>;
+  auto kern = gemm_mxf8_pair<STAGES>;
+  static const cudaError_t attr_err = set_smem_attrs(kern, C::SMEM_BYTES);
+  if (attr_err != cudaSuccess) return attr_err;
+  ka.splits = 1;
+  ka.kb_per_cta = l.k_len / BK;
+  const int64_t tiles = static_cast<int64_t>(l.G) * ceil_div(l.T, 2 * BM) * (l.n_feat / 256);
+  const int max_pairs = num_sms() / 2;
+  const int pairs = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
+  CUtensorMap tma_act, tma_wt, tma_sfa, tma_sfb;
+  if (!make_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&tma_wt, l.wt, static_cast<int64_t>(l.G) * l.n_feat, l.k_len, l.wt_ld, 128)) return cudaErrorInvalidValue;
+  if (!make_sf_map(&tma_sfa, l.act_sf, ceil_div(l.T, 128) * ka.act_gp4)) return cudaErrorInvalidValue;
+  if (!make_sf_map(&tma_sfb, l.wt_sf, ceil_div(static_cast<int64_t>(l.G) * l.n_feat, 128) * ka.wt_gp4))
+    return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(kThreadsPair, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = 2;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  cfg.numAttrs = 1;
+  if (ka.pdl) {
+    attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
+  }
+  cfg.attrs = attrs;
+  return cudaLaunchKernelEx(&cfg, kern, tma_act, tma_wt, tma_sfa, tma_sfb, ka);
+}
+
 cudaError_t launch_gemm(const GemmLaunch& l, cudaStream_t stream) {
   KArgs ka = {};
   ka.T = l.T;
@@ -1010,7 +1336,7 @@ cudaError_t launch_gemm(const GemmLaunch& l, cudaStream_t stream) {
   if (l.T <= 128) return launch_swap<128, 6>(l, ka, stream);
   if (l.T <= 256) return launch_swap<128, 3>(l, ka, stream);
   if (l.T <= kSwapMaxTokens) return launch_swap<128, 3>(l, ka, stream);
-  if (l.n_feat % 256 == 0) return launch_persistent<256, 4>(l, ka, stream);
+  if (l.n_feat % 256 == 0) return launch_pair<6>(l, ka, stream);
   return launch_normal<128, 6>(l, ka, stream);
 }
 
