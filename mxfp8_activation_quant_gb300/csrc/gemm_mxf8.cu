@@ -837,7 +837,8 @@ struct PairCfg {
   static constexpr int A_BYTES = BM * BK;   // this CTA's 128 token rows
   static constexpr int B_BYTES = 128 * BK;  // this CTA's 128 of the 256 weight rows
   static constexpr int SF_BYTES = 512 * 3;  // scale atoms: A (own rows), B (both 128-row atoms)
-  static constexpr int TX_BYTES = 2 * (A_BYTES + B_BYTES + SF_BYTES);  // both CTAs, even CTA's barrier
+  // bytes of one stage of both CTAs (counted on the even CTA's barrier) for a tile of n features
+  __host__ __device__ static constexpr uint32_t tx_bytes(int n) { return 2u * (A_BYTES + (n / 2) * BK + 512 + (n / 128) * 512); }
   static constexpr int OFF_B = STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_BAR = OFF_SF + STAGES * SF_BYTES;
@@ -854,8 +855,8 @@ constexpr int kThreadsPair = 352;  // warp 0 TMA, 1 MMA, 2..9 epilogue, 10 scale
 template <int STAGES>
 __global__ void __launch_bounds__(kThreadsPair, 1)
     gemm_mxf8_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                   const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
-                   const KArgs p) {
+                   const __grid_constant__ CUtensorMap tm_b64, const __grid_constant__ CUtensorMap tm_sfa,
+                   const __grid_constant__ CUtensorMap tm_sfb, const KArgs p) {
   using C = PairCfg<STAGES>;
   constexpr int BN = 256;
   extern __shared__ uint8_t smem_raw[];
@@ -882,17 +883,32 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   const int total = per_group * p.G;
   const int nk = p.kb_per_cta;
   const int first_tile = static_cast<int>(blockIdx.x >> 1), tile_step = static_cast<int>(gridDim.x >> 1);
-  // pair tile -> (group, first token of the 256-token pair tile, first feature)
-  auto decode = [&](int t, int& g, int64_t& m0, int64_t& n0) {
+  // Work items, taken round robin by the pairs: the 256 x 256 tiles of the full waves, then, when
+  // the last wave would leave more than half the pairs idle, its tiles as two 256 x 128 halves
+  // each, which that wave spreads over twice as many pairs.
+  const int tail = total % tile_step;
+  const bool split_tail = tail > 0 && 2 * tail <= tile_step;
+  const int n_items = split_tail ? total + tail : total;
+  // item -> (group, first token of the 256-token pair tile, first feature, features)
+  auto item = [&](int i, int& g, int64_t& m0, int64_t& n0, int& nf) {
+    int t = i, hf = 0;
+    nf = BN;
+    if (split_tail && i >= total - tail) {
+      const int j = i - (total - tail);
+      t = total - tail + (j >> 1);
+      hf = j & 1;
+      nf = BN / 2;
+    }
     g = t / per_group;
     const int r = t - g * per_group;
     m0 = static_cast<int64_t>(r / n_tiles) * (2 * BM);
-    n0 = static_cast<int64_t>(r % n_tiles) * BN;
+    n0 = static_cast<int64_t>(r % n_tiles) * BN + hf * (BN / 2);
   };
 
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_b);
+    tma_prefetch_desc(&tm_b64);
     tma_prefetch_desc(&tm_sfa);
     tma_prefetch_desc(&tm_sfb);
     for (int s = 0; s < STAGES; ++s) {
@@ -923,15 +939,16 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     const uint32_t full0 = mapa_shared(bar_full, 0);  // the even CTA's stage barriers
     int it = 0;
     bool first = true;
-    for (int t = first_tile; t < total && !*abort_flag; t += tile_step) {
-      int g;
+    for (int i = first_tile; i < n_items && !*abort_flag; i += tile_step) {
+      int g, nf;
       int64_t m0, n0;
-      decode(t, g, m0, n0);
+      item(i, g, m0, n0, nf);
+      const uint32_t tx = C::tx_bytes(nf);
       const int64_t a_row = m0 + BM * rank;  // this CTA's token rows
       const int64_t a_x = static_cast<int64_t>(g) * p.act_k_per_group;
       const int64_t a_atom = (a_row >> 7) * p.act_gp4 + (a_x >> 7);  // scale atom of k-block 0
       const int64_t b_first = static_cast<int64_t>(g) * p.n_feat + n0;
-      const int64_t b_row = b_first + 128 * rank;  // this CTA's weight rows
+      const int64_t b_row = b_first + (nf / 2) * rank;  // this CTA's nf / 2 weight rows
       const int64_t b_atom = (b_first >> 7) * p.wt_gp4;
       auto load_act = [&](int s, int kb, uint32_t fb) {
         tma_load_2d_pair(sbase + s * C::A_BYTES, &tm_a, fb, static_cast<int32_t>(a_x + kb * BK), static_cast<int32_t>(a_row));
@@ -939,15 +956,16 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       };
       auto load_wt = [&](int s, int kb, uint32_t fb) {
         const uint32_t sf = sbase + C::OFF_SF + s * C::SF_BYTES;
-        tma_load_2d_pair(sbase + C::OFF_B + s * C::B_BYTES, &tm_b, fb, static_cast<int32_t>(kb * BK), static_cast<int32_t>(b_row));
+        tma_load_2d_pair(sbase + C::OFF_B + s * C::B_BYTES, nf == BN ? &tm_b : &tm_b64, fb,
+                         static_cast<int32_t>(kb * BK), static_cast<int32_t>(b_row));
         tma_load_2d_pair(sf + 512, &tm_sfb, fb, 0, static_cast<int32_t>(b_atom + kb));
-        tma_load_2d_pair(sf + 1024, &tm_sfb, fb, 0, static_cast<int32_t>(b_atom + p.wt_gp4 + kb));
+        if (nf == BN) tma_load_2d_pair(sf + 1024, &tm_sfb, fb, 0, static_cast<int32_t>(b_atom + p.wt_gp4 + kb));
       };
       int kb = 0;
       if (first && p.pdl) {
         const int pre = nk < STAGES ? nk : STAGES;
         for (int j = 0; j < pre; ++j) {
-          if (leader) mbar_arrive_expect_tx(bar_full + 8 * j, C::TX_BYTES);
+          if (leader) mbar_arrive_expect_tx(bar_full + 8 * j, tx);
           load_wt(j, j, full0 + 8 * j);
         }
         pdl_wait_primary();
@@ -964,7 +982,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           report_timeout(p.status);
           break;
         }
-        if (leader) mbar_arrive_expect_tx(bar_full + 8 * s, C::TX_BYTES);
+        if (leader) mbar_arrive_expect_tx(bar_full + 8 * s, tx);
         load_wt(s, kb, full0 + 8 * s);
         load_act(s, kb, full0 + 8 * s);
       }
@@ -977,7 +995,10 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       // soon as the stage's operands have landed: the copies are issued by another thread, so
       // this thread's MMA stream never waits behind a copy of its own.
       int it = 0, ti = 0;
-      for (int t = first_tile; t < total && !*abort_flag; t += tile_step, ++ti) {
+      for (int i = first_tile; i < n_items && !*abort_flag; i += tile_step, ++ti) {
+        int g, nf;
+        int64_t m0, n0;
+        item(i, g, m0, n0, nf);
         if (!mbar_wait_bounded(bar_acce, (ti & 1) ^ 1)) {  // both halves drained by the epilogues
           *abort_flag = 1;
           report_timeout(p.status);
@@ -1000,8 +1021,8 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           const uint64_t bd = sdesc_kmajor_sw128(sbase + C::OFF_B + s * C::B_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
-            tc_mma_mxf8_pair(tmem, ad + 2 * k, bd + 2 * k, idesc_mxf8(2 * BM, BN, k, k), sfa_t, sfb_t,
-                             (kb | k) != 0 ? 1u : 0u);
+            tc_mma_mxf8_pair(tmem, ad + 2 * k, bd + 2 * k, idesc_mxf8(2 * BM, static_cast<uint32_t>(nf), k, k), sfa_t,
+                             sfb_t, (kb | k) != 0 ? 1u : 0u);
           tc_commit_pair(bar_empty + 8 * s, 0x3);
         }
         tc_commit_pair(bar_accf, 0x3);
@@ -1013,22 +1034,24 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   } else if (warp == 10) {
     // ---------------- scale copies (even CTA) ----------------
     if (leader && lane == 0) {
-      const int my_tiles = first_tile < total ? (total - 1 - first_tile) / tile_step + 1 : 0;
-      const int n_iter = my_tiles * nk;
-      for (int it = 0; it < n_iter && !*abort_flag; ++it) {
-        const int s = it % STAGES;
-        if (!mbar_wait_bounded(bar_full + 8 * s, (it / STAGES) & 1)) {
-          *abort_flag = 1;
-          report_timeout(p.status);
-          break;
+      int it = 0;
+      for (int i = first_tile; i < n_items && !*abort_flag; i += tile_step) {
+        const bool full_tile = !(split_tail && i >= total - tail);
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait_bounded(bar_full + 8 * s, (it / STAGES) & 1)) {
+            *abort_flag = 1;
+            report_timeout(p.status);
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sf_src = sbase + C::OFF_SF + s * C::SF_BYTES;
+          const uint32_t sfa_t = tmem + BN + s * C::SF_COLS;
+          tc_cp_sf_atom_pair(sfa_t, sdesc_sf_atom(sf_src));
+          tc_cp_sf_atom_pair(sfa_t + 4, sdesc_sf_atom(sf_src + 512));
+          if (full_tile) tc_cp_sf_atom_pair(sfa_t + 8, sdesc_sf_atom(sf_src + 1024));
+          tc_commit_pair(bar_sf + 8 * s, 0x1);
         }
-        tc_fence_after();
-        const uint32_t sf_src = sbase + C::OFF_SF + s * C::SF_BYTES;
-        const uint32_t sfa_t = tmem + BN + s * C::SF_COLS;
-        tc_cp_sf_atom_pair(sfa_t, sdesc_sf_atom(sf_src));
-        tc_cp_sf_atom_pair(sfa_t + 4, sdesc_sf_atom(sf_src + 512));
-        tc_cp_sf_atom_pair(sfa_t + 8, sdesc_sf_atom(sf_src + 1024));
-        tc_commit_pair(bar_sf + 8 * s, 0x1);
       }
     }
   } else if (warp >= 2) {
@@ -1038,12 +1061,24 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16) + 128 * half;
     const uint32_t acce0 = mapa_shared(bar_acce, 0);
     int ti = 0;
-    for (int t = first_tile; t < total; t += tile_step, ++ti) {
+    for (int i = first_tile; i < n_items; i += tile_step, ++ti) {
+      int g, nf;
+      int64_t m0, n0;
+      item(i, g, m0, n0, nf);
       if (!mbar_wait_bounded(bar_accf, ti & 1)) {
         *abort_flag = 1;
         report_timeout(p.status);
       }
       if (__any_sync(0xffffffffu, *abort_flag)) break;
+      if (128 * half >= nf) {  // a 128-feature item has no columns for half 1
+        if (lane == 0) {
+          if (leader)
+            mbar_arrive(bar_acce);
+          else
+            mbar_arrive_remote(acce0);
+        }
+        continue;
+      }
       tc_fence_after();
       uint32_t acc[4][32];
 #pragma unroll
@@ -1057,9 +1092,6 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         else
           mbar_arrive_remote(acce0);
       }
-      int g;
-      int64_t m0, n0;
-      decode(t, g, m0, n0);
       const int64_t row0 = m0 + BM * rank;
       if (row0 >= p.z_mp128) continue;  // this half of a ragged last pair tile holds no token
       const int64_t row = row0 + 32 * q + lane;
@@ -1277,9 +1309,10 @@ cudaError_t launch_pair(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   const int64_t tiles = static_cast<int64_t>(l.G) * ceil_div(l.T, 2 * BM) * (l.n_feat / 256);
   const int max_pairs = num_sms() / 2;
   const int pairs = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
-  CUtensorMap tma_act, tma_wt, tma_sfa, tma_sfb;
+  CUtensorMap tma_act, tma_wt, tma_wt64, tma_sfa, tma_sfb;
   if (!make_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, BM)) return cudaErrorInvalidValue;
   if (!make_map(&tma_wt, l.wt, static_cast<int64_t>(l.G) * l.n_feat, l.k_len, l.wt_ld, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&tma_wt64, l.wt, static_cast<int64_t>(l.G) * l.n_feat, l.k_len, l.wt_ld, 64)) return cudaErrorInvalidValue;
   if (!make_sf_map(&tma_sfa, l.act_sf, ceil_div(l.T, 128) * ka.act_gp4)) return cudaErrorInvalidValue;
   if (!make_sf_map(&tma_sfb, l.wt_sf, ceil_div(static_cast<int64_t>(l.G) * l.n_feat, 128) * ka.wt_gp4))
     return cudaErrorInvalidValue;
@@ -1300,7 +1333,7 @@ cudaError_t launch_pair(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
     cfg.numAttrs = 2;
   }
   cfg.attrs = attrs;
-  return cudaLaunchKernelEx(&cfg, kern, tma_act, tma_wt, tma_sfa, tma_sfb, ka);
+  return cudaLaunchKernelEx(&cfg, kern, tma_act, tma_wt, tma_wt64, tma_sfa, tma_sfb, ka);
 }
 
 cudaError_t launch_gemm(const GemmLaunch& l, cudaStream_t stream) {
