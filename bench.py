@@ -129,6 +129,30 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ---- ranks (replicas only: one process per GPU, no collective on the data path) ---------------
+def rank_env():
+    """(world size, rank, local rank) from the torchrun environment; (1, 0, 0) without it."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value, world, device):
+    """The largest `value` over all ranks (all-reduce MAX); `value` itself with one rank."""
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, tokens_per_rank, steps, max_ms):
+    """Tokens per second of the whole job: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (max_ms / 1e3)
+
+
 # ---- the GPU arm -------------------------------------------------------------------------------
 def run_gpu(args):
     import torch
@@ -137,9 +161,7 @@ def run_gpu(args):
     import mxfp8_activation_quant_gb300 as mxq
     from mxfp8_activation_quant_gb300 import synth
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if world > 1:
@@ -212,13 +234,9 @@ def run_gpu(args):
 
     parts = [[evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)] for j in range(4)]
     step_ms = [sum(parts[j][i] for j in range(4)) for i in range(args.steps)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
-    tokens_per_s = world * T * args.steps / (total_ms / 1e3)
+    tokens_per_s = whole_job_rate(world, T, args.steps, total_ms)
 
     # end-to-end through the public API: pinned host inputs -> device -> chain -> host result
     x_h = x.cpu().pin_memory()
@@ -244,12 +262,8 @@ def run_gpu(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_tps = world * T * args.steps / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_tps = whole_job_rate(world, T, args.steps, e2e_ms)
 
     hbm, bf16_tf, peak_kind = load_peaks()
     mx_tf = 2.0 * bf16_tf  # fp8 dense rate = 2x bf16 (nominal 4.5 / 2.25 PFLOP/s)
@@ -475,9 +489,10 @@ def cpu_baseline(args, T, budget_s=15.0):
 
 
 def run_reference(args):
-    """The reference arm: the CPU oracle timed on this machine's host cores, rank 0 only."""
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    if int(os.environ.get("RANK", "0")) != 0:
+    """The reference arm: the CPU oracle timed on this machine's host cores, rank 0 only (the other
+    ranks return at once, without work)."""
+    world, rank, _ = rank_env()
+    if rank != 0:
         return
     import oracle
 

@@ -10,6 +10,8 @@ Overview / Validation / Details).
   * the whole _o_proj output within 1e-2 relative Frobenius of the oracle's own chain.
 Token counts follow the pages' tests: 1, 129, 8193 tokens and M in {1, 4, 7, 64, 300}, plus the
 decode and prefill sweeps."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -226,6 +228,60 @@ def test_o_proj_graph_replay(mxq, weights):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(zq2, zq) and torch.equal(ztl2, ztl) and torch.equal(out2, out)
+
+
+def _kernel_nodes(graph):
+    """Kernel nodes of a captured CUDA graph, counted through the driver API."""
+    cu = ctypes.CDLL("libcuda.so.1")
+    h = ctypes.c_void_p(graph.raw_cuda_graph())
+    n = ctypes.c_size_t(0)
+    assert cu.cuGraphGetNodes(h, None, ctypes.byref(n)) == 0
+    nodes = (ctypes.c_void_p * n.value)()
+    assert cu.cuGraphGetNodes(h, nodes, ctypes.byref(n)) == 0
+    kinds = []
+    for i in range(n.value):
+        t = ctypes.c_int(-1)
+        assert cu.cuGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t)) == 0
+        kinds.append(t.value)
+    return sum(k == 0 for k in kinds), len(kinds)  # CU_GRAPH_NODE_TYPE_KERNEL == 0
+
+
+@pytest.mark.parametrize("T", [1, 256, 4096])
+def test_fused_chain_launches_two_kernels(mxq, weights, T):
+    """No standalone quantize launch in the fused path: a captured o_proj_mxfp8 holds exactly two
+    kernels (wo_a, wo_b), and the unfused chain (wo_a writing bf16 z, the quantizer, wo_b) three."""
+    from mxfp8_activation_quant_gb300 import synth
+
+    try:
+        g1, g2 = torch.cuda.CUDAGraph(keep_graph=True), torch.cuda.CUDAGraph(keep_graph=True)
+    except TypeError:
+        pytest.skip("this torch cannot keep the captured graph")
+    O = gpu_mx(mxq, synth.o_proj_activation(3, T))
+    zq = torch.empty((T, synth.KB), dtype=torch.uint8, device="cuda")
+    ztl = mxq.empty_sf(2, T, synth.KB)
+    zb = torch.empty((T, synth.KB), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((T, synth.NB), dtype=torch.bfloat16, device="cuda")
+    Z = mxq.MXFP8(zq, ztl)
+
+    def fused():
+        mxq.o_proj_mxfp8(O, weights.WA, weights.WB, T, synth.G, synth.NA, synth.KA, synth.NB, zq, ztl, out)
+
+    def unfused():
+        mxq.wo_a_einsum_mxfp8(O, weights.WA, T, synth.G, synth.NA, synth.KA, z_bf16=zb)
+        mxq.mxfp8_quantize(zb, zq, None, None, ztl)
+        mxq.gemm_mxfp8_bf16(Z, weights.WB, out)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fused()
+        unfused()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g1):
+        fused()
+    with torch.cuda.graph(g2):
+        unfused()
+    assert _kernel_nodes(g1) == (2, 2)
+    assert _kernel_nodes(g2) == (3, 3)
 
 
 def test_status_word_stays_clear(mxq, weights):
