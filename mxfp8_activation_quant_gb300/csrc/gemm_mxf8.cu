@@ -13,7 +13,7 @@
 // Two orientations:
 //   normal  (large T): A = activations (128 tokens / tile), B = weights (BN features / tile).
 //           TMEM lane = token row, so one thread holds a 32-column quantization group.
-//   swap-AB (T <= 512): A = weights (128 features / tile), B = activations (one token tile of
+//   swap-AB (T <= 384): A = weights (128 features / tile), B = activations (one token tile of
 //           N = 16..64, or 128-token tiles). TMEM lane = feature, so a quantization group is
 //           one warp (32 lanes). The K range is split over a thread-block cluster; partial sums
 //           meet in distributed shared memory and are added in fixed rank order
@@ -38,7 +38,7 @@ constexpr int kThreads = 192;
 constexpr int BM = 128;            // MMA M: rows of the A operand = TMEM lanes
 constexpr int BK = 128;            // K bytes per stage = one 128-byte swizzle row
 constexpr int kStatusTimeout = 6;  // MXQ_ERR_TIMEOUT
-constexpr int kSwapMaxTokens = 512; // above this the normal orientation reuses operands better
+constexpr int kSwapMaxTokens = 384; // above this the CTA-pair kernel is faster (measured, T = 512)
 
 struct KArgs {
   int64_t T;
@@ -1308,7 +1308,10 @@ cudaError_t launch_pair(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   ka.kb_per_cta = l.k_len / BK;
   const int64_t tiles = static_cast<int64_t>(l.G) * ceil_div(l.T, 2 * BM) * (l.n_feat / 256);
   const int max_pairs = num_sms() / 2;
-  const int pairs = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
+  // With fewer tiles than half the pairs, launch two pairs per tile: the kernel then runs every
+  // tile as two 256 x 128 halves (its last-wave split), one per pair.
+  const int64_t want = 2 * tiles <= max_pairs ? 2 * tiles : tiles;
+  const int pairs = static_cast<int>(want < max_pairs ? want : max_pairs);
   CUtensorMap tma_act, tma_wt, tma_wt64, tma_sfa, tma_sfb;
   if (!make_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, BM)) return cudaErrorInvalidValue;
   if (!make_map(&tma_wt, l.wt, static_cast<int64_t>(l.G) * l.n_feat, l.k_len, l.wt_ld, 128)) return cudaErrorInvalidValue;
