@@ -41,6 +41,7 @@ TID_QX_ELEM = 12
 TID_RMS_X = 20
 TID_RMS_GAMMA = 21
 TID_RMS_OUTLIER = 22
+TID_WQKV = 30
 
 # DeepSeek-V4.1 _o_proj shapes at TP1
 G, NA, KA, NB = 8, 1024, 4096, 5120
@@ -178,6 +179,16 @@ def wo_a_weight(seed: int, device="cpu") -> torch.Tensor:
 def wo_b_weight(seed: int, device="cpu") -> torch.Tensor:
     """wo_b, bf16 [NB, G*NA] = [5120, 8192] ~ N(0, 1/sqrt(8192))."""
     return normal_bf16(seed, TID_WB, NB, KB, 1.0 / math.sqrt(KB), device=device)
+
+
+# The down-projection that consumes RMSNorm's MXFP8 y ("fused_wqa_wkv"). The pages do not give
+# its width; 2048 output features (a multiple of the 128-row weight tile) stand in for it.
+WQKV_N = 2048
+
+
+def wqa_wkv_weight(seed: int, N: int = WQKV_N, H: int = RMS_H, device="cpu") -> torch.Tensor:
+    """fused_wqa_wkv stand-in, bf16 [N, H] ~ N(0, 1/sqrt(H))."""
+    return normal_bf16(seed, TID_WQKV, N, H, 1.0 / math.sqrt(H), device=device)
 
 
 # ---- standalone quantizer input ----------------------------------------------------------
