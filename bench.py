@@ -419,6 +419,14 @@ def sweep(args, mxq, synth, torch, dev, WA, WB):
             mxq.gemm_mxfp8_bf16(mxq.MXFP8(zq, zsf), WB, out)
 
         unf = timeit(unfused)
+        extra = {}
+        if T <= 16:  # bf16 o quantized inside wo_a, against the quantize launch + the fused pair
+            ob = synth.o_proj_activation(0, T, device=dev)
+            extra["from_bf16_us"] = round(timeit(lambda: mxq.o_proj_mxfp8_from_bf16(
+                ob, WA, WB, T, G, NA, KA, NB, zq, zsf, out)), 3)
+            extra["quantize_then_fused_us"] = round(timeit(lambda: (mxq.mxfp8_quantize(ob, oq, None, None, osf[2]),
+                                                                    mxq.o_proj_mxfp8(O, WA, WB, T, G, NA, KA, NB,
+                                                                                     zq, zsf, out))), 3)
         wa_us = timeit(lambda: mxq.wo_a_einsum_mxfp8(O, WA, T, G, NA, KA, z_q=zq, z_sf_128x4=zsf))
         wb_us = timeit(lambda: mxq.gemm_mxfp8_bf16(mxq.MXFP8(zq, zsf), WB, out))
         byts = WEIGHT_BYTES + T * (G * KA * 33 // 32 + 2 * KB * 33 // 32 + NB * 2)
@@ -427,7 +435,7 @@ def sweep(args, mxq, synth, torch, dev, WA, WB):
                           "saving_us": round(unf - fused, 3), "wo_a_us": round(wa_us, 3), "wo_b_us": round(wb_us, 3),
                           "TFLOP/s": round(FLOP_PER_TOKEN * T / fused / 1e6, 1), "roofline_us": round(roof, 3),
                           "frac": round(roof / fused, 4),
-                          "weight_GB/s": round(WEIGHT_BYTES / fused / 1e3, 1)}), flush=True)
+                          "weight_GB/s": round(WEIGHT_BYTES / fused / 1e3, 1), **extra}), flush=True)
         del oq, osf, O, zq, zsf, zb, out
 
 

@@ -187,6 +187,20 @@ MXQ_API mxq_status o_proj_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa,
                                 void* status, void* stream);
 
 /*
+ * o_proj_mxfp8_from_bf16 -- the _o_proj pair at decode sizes (T <= 16) fed by bf16 o
+ * ([KeepMXFP8] Pieces: the small-M wo_a that quantizes its activation in the kernel, "pre-quantized
+ * == in-kernel"). wo_a loads o as bf16 and quantizes each tile in shared memory with exactly the
+ * rule of mxfp8_quantize, so z, its scales and out are bit-identical to mxfp8_quantize(o) followed
+ * by o_proj_mxfp8; no quantize launch for o either.
+ *   o_bf16 : bf16 [T, G * Ka], row stride ld_o elements (ld_o * 2 a multiple of 16 bytes).
+ * Other arguments as in o_proj_mxfp8. T > 16 returns MXQ_ERR_UNSUPPORTED_SHAPE.
+ */
+MXQ_API mxq_status o_proj_mxfp8_from_bf16(const void* o_bf16, int64_t ld_o, const mxq_mx_tensor* wa,
+                                          const mxq_mx_tensor* wb, int64_t T, int32_t G, int32_t Na, int32_t Ka,
+                                          int32_t Nb, void* z_q, void* z_sf_128x4, void* z_sf_packed_i32,
+                                          void* z_bf16, void* out_bf16, void* status, void* stream);
+
+/*
  * o_proj_mxfp8_noalloc -- o_proj_mxfp8 with the z hand-off held in a fixed buffer inside the
  * library, so the caller passes no z buffers and nothing is allocated. The pages have no
  * counterpart: they always hand z over in a caller-owned tensor.

@@ -15,6 +15,7 @@ from ._lib import (  # noqa: F401
     mxfp8_quantize,
     new_status,
     o_proj_mxfp8,
+    o_proj_mxfp8_from_bf16,
     o_proj_mxfp8_noalloc,
     quantize,
     rmsnorm_dual_out,

@@ -59,6 +59,7 @@ SIGNATURES = {
     "gemm_mxfp8_bf16": ([_MXP, _MXP, I64, I64, I64, P, I64, P, P], ctypes.c_int),
     "o_proj_mxfp8": ([_MXP, _MXP, _MXP, I64, I32, I32, I32, I32, P, P, P, P, P, P, P], ctypes.c_int),
     "o_proj_mxfp8_noalloc": ([_MXP, _MXP, _MXP, I64, I32, I32, I32, I32, P, P, P], ctypes.c_int),
+    "o_proj_mxfp8_from_bf16": ([P, I64, _MXP, _MXP, I64, I32, I32, I32, I32, P, P, P, P, P, P, P], ctypes.c_int),
 }
 
 # capacity of the library-held z buffer of o_proj_mxfp8_noalloc (include/mxq.h)
@@ -204,3 +205,14 @@ def o_proj_mxfp8_noalloc(o: MXFP8, wa: MXFP8, wb: MXFP8, T: int, G: int, Na: int
     oc, ac, bc = o.c(), wa.c(), wb.c()
     _check(load().o_proj_mxfp8_noalloc(ctypes.byref(oc), ctypes.byref(ac), ctypes.byref(bc), T, G, Na, Ka, Nb,
                                        _ptr(out), _ptr(status), _stream(stream)), "o_proj_mxfp8_noalloc")
+
+
+def o_proj_mxfp8_from_bf16(o: torch.Tensor, wa: MXFP8, wb: MXFP8, T: int, G: int, Na: int, Ka: int, Nb: int, z_q,
+                           z_sf_128x4, out: torch.Tensor, z_sf_packed=None, z_bf16=None, status=None,
+                           stream=None) -> None:
+    """The _o_proj pair from bf16 o (T <= 16): wo_a quantizes o in the kernel."""
+    assert o.dtype == torch.bfloat16 and o.dim() == 2 and o.stride(1) == 1
+    ac, bc = wa.c(), wb.c()
+    _check(load().o_proj_mxfp8_from_bf16(_ptr(o), o.stride(0), ctypes.byref(ac), ctypes.byref(bc), T, G, Na, Ka, Nb,
+                                         _ptr(z_q), _ptr(z_sf_128x4), _ptr(z_sf_packed), _ptr(z_bf16), _ptr(out),
+                                         _ptr(status), _stream(stream)), "o_proj_mxfp8_from_bf16")

@@ -68,14 +68,20 @@ __device__ __forceinline__ void report_timeout(int32_t* status) {
   if (status != nullptr) atomicCAS(status, 0, kStatusTimeout);
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool CVT = false>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK;
   static constexpr int B_BYTES = BN * BK;
   static constexpr int SFB_ATOMS = (BN + 127) / 128;
   static constexpr int SF_BYTES = 512 * (1 + SFB_ATOMS);
   static constexpr int SF_COLS = 16;  // TMEM columns per stage slot (4 for A + 4 per B atom, padded)
-  static constexpr int TX_BYTES = A_BYTES + B_BYTES + SF_BYTES;
+  // CVT: the activation tile arrives as bf16 (BN rows of 128 elements, 256-byte rows, no
+  // swizzle) in a staging slot, and the epilogue warps quantize it into the B tile and its
+  // scale atom before the MMAs of the stage
+  static constexpr int BF_BYTES = CVT ? BN * 256 : 0;
+  // bytes on the stage's full barrier; with CVT the bf16 tile has a barrier of its own, so the
+  // quantization starts as soon as it lands, under the larger weight load
+  static constexpr int TX_BYTES = CVT ? A_BYTES + 512 : A_BYTES + B_BYTES + SF_BYTES;
   static constexpr int OFF_B = STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
   // Split-K reduction (swap-AB). Token tiles of 16 columns (decode) push their partials
@@ -87,9 +93,11 @@ struct Cfg {
   static constexpr bool PUSH = BN <= 16;
   static constexpr int RECV_BYTES = PUSH ? 128 * BN * 4 : 0;
   static constexpr bool split_fits(int s) { return PUSH || BN * 512 + BN * 512 / s * (s - 1) <= OFF_SF; }
-  static constexpr int OFF_RECV = OFF_SF + STAGES * SF_BYTES;
+  static constexpr int OFF_BF = OFF_SF + STAGES * SF_BYTES;
+  static constexpr int OFF_RECV = OFF_BF + STAGES * BF_BYTES;
   static constexpr int OFF_BAR = OFF_RECV + RECV_BYTES;
-  static constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 4) * 8;  // full, empty, 4 more
+  // full, empty, 4 more, and (CVT) "converted" and "bf16 landed" barriers per stage
+  static constexpr int OFF_MISC = OFF_BAR + ((CVT ? 4 : 2) * STAGES + 4) * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr int TMEM_USED = BN + STAGES * SF_COLS;
   static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
@@ -206,11 +214,12 @@ __device__ __forceinline__ void epi_token_group(const KArgs& p, const float (&v)
   }
 }
 
-template <int BN, int STAGES, bool SWAP>
+template <int BN, int STAGES, bool SWAP, bool CVT = false>
 __global__ void __launch_bounds__(kThreads, 3)
     gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                      const KArgs p) {
-  using C = Cfg<BN, STAGES>;
+  static_assert(!CVT || (SWAP && BN == 16), "in-kernel activation quantization: decode tiles only");
+  using C = Cfg<BN, STAGES, CVT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sraw = smem_u32(smem_raw);
   const uint32_t sbase = (sraw + 1023u) & ~1023u;  // 128-byte-swizzled tiles need 1024-byte alignment
@@ -219,6 +228,8 @@ __global__ void __launch_bounds__(kThreads, 3)
   const uint32_t bar_empty = bar_full + STAGES * 8;  // STAGES x 8 B
   const uint32_t bar_accf = bar_empty + STAGES * 8;  // 8 B
   const uint32_t bar_recv = bar_accf + 8;            // 8 B: split-K partials received
+  const uint32_t bar_conv = bar_full + (2 * STAGES + 4) * 8;  // CVT: STAGES x 8 B, stage quantized
+  const uint32_t bar_act = bar_conv + STAGES * 8;             // CVT: STAGES x 8 B, bf16 tile landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   int* issued_cnt = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
@@ -277,6 +288,11 @@ __global__ void __launch_bounds__(kThreads, 3)
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_accf, 1);
+    if (CVT)
+      for (int s = 0; s < STAGES; ++s) {
+        mbar_init(bar_conv + 8 * s, 4);  // one arrival per epilogue warp
+        mbar_init(bar_act + 8 * s, 1);
+      }
     if (SWAP && p.splits > 1) {
       mbar_init(bar_recv, 1);
       // PUSH: every rank, this one included, sends 128 features x (BN / splits) columns of fp32;
@@ -309,7 +325,12 @@ __global__ void __launch_bounds__(kThreads, 3)
     const uint32_t a_dst0 = sbase, b_dst0 = sbase + C::OFF_B, sf_dst0 = sbase + C::OFF_SF;
     // operand loads of k-block i into stage s; the weight operand is A in swap-AB, B otherwise
     auto load_act = [&](int s, int kb, uint32_t fb) {
-      if (SWAP) {
+      if (SWAP && CVT) {  // bf16 activations (element coordinates) into the staging slot
+        const uint32_t ab = bar_act + (fb - bar_full);
+        mbar_arrive_expect_tx(ab, C::BF_BYTES);
+        tma_load_2d(sbase + C::OFF_BF + s * C::BF_BYTES, &tm_b, ab, static_cast<int32_t>(b_xoff + kb * BK),
+                    static_cast<int32_t>(b_row0));
+      } else if (SWAP) {
         tma_load_2d(b_dst0 + s * C::B_BYTES, &tm_b, fb, static_cast<int32_t>(b_xoff + kb * BK), static_cast<int32_t>(b_row0));
 #pragma unroll
         for (int j = 0; j < C::SFB_ATOMS; ++j)
@@ -365,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       const int s = i % STAGES;
       const uint32_t ph = (i / STAGES) & 1;
       if (*abort_flag) break;
-      if (!mbar_wait_bounded(bar_full + 8 * s, ph)) {
+      if (!mbar_wait_bounded(bar_full + 8 * s, ph) || (CVT && !mbar_wait_bounded(bar_conv + 8 * s, ph))) {
         *abort_flag = 1;
         report_timeout(p.status);
         break;
@@ -393,6 +414,38 @@ __global__ void __launch_bounds__(kThreads, 3)
   const bool epi = warp >= 2;
   const int q = warp & 3;  // TMEM lane quarter this warp may access
   const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16);
+  if (CVT && epi) {
+    // During the mainloop the epilogue warps quantize each stage's bf16 activations exactly as
+    // mxfp8_quantize does: thread t takes token row t / 8 and 16 elements of group (t / 2) % 4;
+    // the two halves of a group meet by one shuffle for the amax.
+    const int t = static_cast<int>(threadIdx.x) - 64;
+    const int r = t >> 3, c = (t >> 1) & 3, h = t & 1;
+    // rows >= 16 of the activation scale atoms stay zero
+    for (int i = t; i < STAGES * 128; i += 128)
+      reinterpret_cast<uint32_t*>(smem + C::OFF_SF + (i >> 7) * C::SF_BYTES + 512)[i & 127] = 0u;
+    named_barrier(3, 128);
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % STAGES;
+      if (!mbar_wait_bounded(bar_act + 8 * s, (i / STAGES) & 1)) {
+        *abort_flag = 1;
+        report_timeout(p.status);
+        break;
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(smem + C::OFF_BF + s * C::BF_BYTES + r * 256 + (32 * c + 16 * h) * 2);
+      const uint4 v0 = src[0], v1 = src[1];
+      uint32_t am = max(absmax8(v0), absmax8(v1));
+      am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
+      const uint32_t code = ue8m0_from_bf16_amax(am);
+      const float sc = ue8m0_inverse(code);
+      const uint2 q0 = quant8(v0, sc), q1 = quant8(v1, sc);
+      const int j = 2 * c + h;  // 16-byte chunk of the 128-byte row, 128-byte swizzle
+      st_smem_v4(sbase + C::OFF_B + s * C::B_BYTES + r * 128 + ((j ^ (r & 7)) << 4), q0.x, q0.y, q1.x, q1.y);
+      if (h == 0) smem[C::OFF_SF + s * C::SF_BYTES + 512 + r * 16 + c] = static_cast<uint8_t>(code);
+      fence_proxy_async_smem();  // the MMA and the scale copy read these through the async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_conv + 8 * s);
+    }
+  }
   if (epi) {
     if (!mbar_wait_bounded(bar_accf, 0)) {
       *abort_flag = 1;
@@ -600,8 +653,10 @@ __global__ void __launch_bounds__(kThreads, 3)
   __syncthreads();
   if (*abort_flag) {
     if (warp == 0 && lane == 0) {
-      for (int i = *consumed_cnt; i < *issued_cnt; ++i)
+      for (int i = *consumed_cnt; i < *issued_cnt; ++i) {
         (void)mbar_wait_bounded(bar_full + 8 * (i % STAGES), (i / STAGES) & 1);
+        if (CVT) (void)mbar_wait_bounded(bar_act + 8 * (i % STAGES), (i / STAGES) & 1);
+      }
     }
     if (warp == 1 && lane == 0) (void)mbar_wait_bounded(bar_accf, 0);
     __syncthreads();
@@ -1181,6 +1236,20 @@ bool make_sf_map(CUtensorMap* m, const void* base, int64_t atoms) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 activations [rows, cols] (row stride ld elements) in boxes of 128 elements x box_rows,
+// unswizzled: 256-byte rows in shared memory.
+bool make_bf16_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int num_sms() {
   int dev = 0, n = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
@@ -1189,22 +1258,26 @@ int num_sms() {
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool CVT = false>
 int ctas_per_sm() {
-  using C = Cfg<BN, STAGES>;
+  using C = Cfg<BN, STAGES, CVT>;
   const int by_smem = C::SM_SMEM / (C::SMEM_LAUNCH + 1024);
   const int by_tmem = 512 / C::TMEM_COLS;
   return by_smem < by_tmem ? by_smem : by_tmem;
 }
 
-template <int BN, int STAGES, bool SWAP>
+template <int BN, int STAGES, bool SWAP, bool CVT = false>
 cudaError_t launch_cfg(const GemmLaunch& l, const KArgs& ka, dim3 grid, int cluster_z, cudaStream_t stream) {
-  using C = Cfg<BN, STAGES>;
-  auto kern = gemm_mxf8_kernel<BN, STAGES, SWAP>;
+  using C = Cfg<BN, STAGES, CVT>;
+  auto kern = gemm_mxf8_kernel<BN, STAGES, SWAP, CVT>;
   static const cudaError_t attr_err = set_smem_attrs(kern, C::SMEM_LAUNCH);
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap tma_act, tma_wt;
-  if (!make_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, SWAP ? BN : BM)) return cudaErrorInvalidValue;
+  if (CVT) {
+    if (!make_bf16_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, BN)) return cudaErrorInvalidValue;
+  } else if (!make_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, SWAP ? BN : BM)) {
+    return cudaErrorInvalidValue;
+  }
   if (!make_map(&tma_wt, l.wt, static_cast<int64_t>(l.G) * l.n_feat, l.k_len, l.wt_ld, SWAP ? BM : BN))
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
@@ -1234,26 +1307,26 @@ cudaError_t launch_cfg(const GemmLaunch& l, const KArgs& ka, dim3 grid, int clus
 // Largest split of the K range (cluster size) that divides the k-blocks, leaves every rank at
 // least 4 token columns, fits its staging in shared memory and keeps every CTA resident in one
 // wave.
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool CVT = false>
 int pick_splits(int tiles, int kb_total, int slots) {
   for (int s = 8; s > 1; s >>= 1)
-    if (kb_total % s == 0 && BN / s >= 4 && Cfg<BN, STAGES>::split_fits(s) && tiles * s <= slots) return s;
+    if (kb_total % s == 0 && BN / s >= 4 && Cfg<BN, STAGES, CVT>::split_fits(s) && tiles * s <= slots) return s;
   return 1;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool CVT = false>
 cudaError_t launch_swap(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   const int tok_tiles = static_cast<int>(ceil_div(l.T, BN));
   const int tiles = l.G * (l.n_feat / BM) * tok_tiles;
   const int kb_total = l.k_len / BK;
-  const int slots = num_sms() * ctas_per_sm<BN, STAGES>();
-  const int s = pick_splits<BN, STAGES>(tiles, kb_total, slots);
+  const int slots = num_sms() * ctas_per_sm<BN, STAGES, CVT>();
+  const int s = pick_splits<BN, STAGES, CVT>(tiles, kb_total, slots);
   ka.splits = s;
   ka.kb_per_cta = kb_total / s;
   ka.per_rank_shift = 0;
   while ((1 << ka.per_rank_shift) < BN / s) ++ka.per_rank_shift;
   dim3 grid(static_cast<unsigned>(l.n_feat / BM), static_cast<unsigned>(tok_tiles), static_cast<unsigned>(l.G * s));
-  return launch_cfg<BN, STAGES, true>(l, ka, grid, s, stream);
+  return launch_cfg<BN, STAGES, true, CVT>(l, ka, grid, s, stream);
 }
 
 template <int BN, int STAGES>
@@ -1366,6 +1439,10 @@ cudaError_t launch_gemm(const GemmLaunch& l, cudaStream_t stream) {
   // T <= 16: a grid followed by a dependent (wo_a of o_proj_mxfp8) uses 3 stages so that the
   // dependent wo_b CTAs that find room start early and fetch their first weight stages; other
   // grids keep 5 stages, about 14 MB of loads in flight
+  if (l.act_is_bf16) {  // bf16 activations, quantized in the kernel: decode tiles only
+    if (l.T > 16) return cudaErrorInvalidValue;
+    return launch_swap<16, 3, true>(l, ka, stream);
+  }
   if (l.T <= 16) return l.has_dependent ? launch_swap<16, 3>(l, ka, stream) : launch_swap<16, 5>(l, ka, stream);
   if (l.T <= 32) return launch_swap<32, 5>(l, ka, stream);
   if (l.T <= 64) return launch_swap<64, 4>(l, ka, stream);

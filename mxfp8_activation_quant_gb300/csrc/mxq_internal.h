@@ -62,6 +62,9 @@ struct GemmLaunch {
   // A programmatic dependent grid follows this one (wo_a inside o_proj_mxfp8): prefer a
   // lighter per-CTA footprint so that the dependent's CTAs can be resident alongside.
   bool has_dependent;
+  // act is bf16 [T, act_cols] (row stride act_ld elements), quantized to MXFP8 inside the
+  // kernel with mxfp8_quantize's rule; act_sf is unused. T <= 16 only.
+  bool act_is_bf16;
 };
 cudaError_t launch_gemm(const GemmLaunch& a, cudaStream_t stream);
 

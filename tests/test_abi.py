@@ -27,7 +27,7 @@ def test_every_declared_symbol_is_exported(lib):
     from mxfp8_activation_quant_gb300 import _lib
 
     names = declared_functions()
-    assert len(names) == 12, names
+    assert len(names) == 13, names
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(_lib.SIGNATURES)
@@ -116,3 +116,19 @@ def test_o_proj_noalloc_argument_errors(lib):
                  None) == 2
     assert n(B(mx(0, 32768)), B(mx(8192, 4096)), B(mx(5120, 8192)), 0, 8, 1024, 4096, 5120, FAKE, None, None) == 1
     assert n(B(mx(4, 32768)), B(mx(8192, 4096)), B(mx(5120, 8192)), 4, 8, 1000, 4096, 5120, FAKE, None, None) == 2
+
+
+def test_o_proj_from_bf16_argument_errors(lib):
+    from mxfp8_activation_quant_gb300._lib import MxTensorC
+
+    def mx(rows, cols):
+        return MxTensorC(FAKE, FAKE, 2, rows, cols, cols)
+
+    B = ctypes.byref
+    f = lib.o_proj_mxfp8_from_bf16
+    args = (B(mx(8192, 4096)), B(mx(5120, 8192)))
+    assert f(FAKE, 32768, *args, 17, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, None, None) == 2  # T > 16
+    assert f(None, 32768, *args, 4, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, None, None) == 1
+    assert f(FAKE, 32000, *args, 4, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, None, None) == 2  # ld_o
+    assert f(FAKE + 2, 32768, *args, 4, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, None, None) == 3
+    assert f(FAKE, 32772, *args, 4, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, None, None) == 3  # ld_o*2 % 16

@@ -284,6 +284,36 @@ def test_fused_chain_launches_two_kernels(mxq, weights, T):
     assert _kernel_nodes(g2) == (3, 3)
 
 
+@pytest.mark.parametrize("T,pad", [(1, 0), (2, 0), (7, 64), (16, 0)])
+def test_o_proj_from_bf16_matches_prequantized(mxq, weights, T, pad):
+    """wo_a quantizing bf16 o in the kernel gives the same bytes as mxfp8_quantize(o) followed
+    by o_proj_mxfp8: z, both scale layouts, the bf16 z and out (the pages' "pre-quantized ==
+    in-kernel"). `pad` extra columns make o a strided view."""
+    from mxfp8_activation_quant_gb300 import synth
+
+    o_full = torch.zeros((T, synth.G * synth.KA + pad), dtype=torch.bfloat16, device="cuda")
+    o = o_full[:, : synth.G * synth.KA]
+    o.copy_(synth.o_proj_activation(8, T, device="cuda"))
+    st = mxq.new_status()
+
+    def bufs():
+        return (torch.empty((T, synth.KB), dtype=torch.uint8, device="cuda"), mxq.empty_sf(2, T, synth.KB),
+                mxq.empty_sf(1, T, synth.KB), torch.empty((T, synth.KB), dtype=torch.bfloat16, device="cuda"),
+                torch.empty((T, synth.NB), dtype=torch.bfloat16, device="cuda"))
+
+    a = bufs()
+    mxq.o_proj_mxfp8_from_bf16(o, weights.WA, weights.WB, T, synth.G, synth.NA, synth.KA, synth.NB, a[0], a[1], a[4],
+                               z_sf_packed=a[2], z_bf16=a[3], status=st)
+    b = bufs()
+    O = gpu_mx(mxq, o.contiguous())
+    mxq.o_proj_mxfp8(O, weights.WA, weights.WB, T, synth.G, synth.NA, synth.KA, synth.NB, b[0], b[1], b[4],
+                     z_sf_packed=b[2], z_bf16=b[3], status=st)
+    torch.cuda.synchronize()
+    mxq.check_status(st)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
 def test_status_word_stays_clear(mxq, weights):
     from mxfp8_activation_quant_gb300 import synth
 
