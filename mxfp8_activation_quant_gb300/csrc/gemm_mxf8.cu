@@ -62,26 +62,35 @@ struct KArgs {
   uint8_t* z_sf_pk;  // byte view of the packed words
   int64_t z_mp4;
   int32_t* status;
+  int64_t act_mp4;  // packed activation scales: rows per word column (ceil(T / 4) * 4)
 };
 
 __device__ __forceinline__ void report_timeout(int32_t* status) {
   if (status != nullptr) atomicCAS(status, 0, kStatusTimeout);
 }
 
-template <int BN, int STAGES, bool CVT = false>
+// How the activation operand of the swap-AB kernel arrives: MXFP8 with F8_128x4 scales (the
+// default), bf16 quantized in the kernel, or MXFP8 with int32-packed MN-major scales rearranged
+// into the F8_128x4 atom in the kernel. The last two are decode tiles only (BN = 16).
+constexpr int kActMx = 0, kActBf16 = 1, kActPackedSf = 2;
+
+template <int BN, int STAGES, int ACT = kActMx>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK;
   static constexpr int B_BYTES = BN * BK;
   static constexpr int SFB_ATOMS = (BN + 127) / 128;
   static constexpr int SF_BYTES = 512 * (1 + SFB_ATOMS);
   static constexpr int SF_COLS = 16;  // TMEM columns per stage slot (4 for A + 4 per B atom, padded)
-  // CVT: the activation tile arrives as bf16 (BN rows of 128 elements, 256-byte rows, no
+  // kActBf16: the activation tile arrives as bf16 (BN rows of 128 elements, 256-byte rows, no
   // swizzle) in a staging slot, and the epilogue warps quantize it into the B tile and its
-  // scale atom before the MMAs of the stage
-  static constexpr int BF_BYTES = CVT ? BN * 256 : 0;
-  // bytes on the stage's full barrier; with CVT the bf16 tile has a barrier of its own, so the
-  // quantization starts as soon as it lands, under the larger weight load
-  static constexpr int TX_BYTES = CVT ? A_BYTES + 512 : A_BYTES + B_BYTES + SF_BYTES;
+  // scale atom before the MMAs of the stage. kActPackedSf: the B tile arrives as usual and the
+  // BN packed scale words of the stage land in the staging slot, which the epilogue warps
+  // scatter into the atom.
+  static constexpr int BF_BYTES = ACT == kActBf16 ? BN * 256 : ACT == kActPackedSf ? BN * 4 : 0;
+  // bytes on the stage's full barrier; the staged activation part has a barrier of its own, so
+  // its conversion starts as soon as it lands, under the larger weight load
+  static constexpr int TX_BYTES = ACT == kActBf16 ? A_BYTES + 512 : ACT == kActPackedSf ? A_BYTES + B_BYTES + 512
+                                                                                       : A_BYTES + B_BYTES + SF_BYTES;
   static constexpr int OFF_B = STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
   // Split-K reduction (swap-AB). Token tiles of 16 columns (decode) push their partials
@@ -96,8 +105,8 @@ struct Cfg {
   static constexpr int OFF_BF = OFF_SF + STAGES * SF_BYTES;
   static constexpr int OFF_RECV = OFF_BF + STAGES * BF_BYTES;
   static constexpr int OFF_BAR = OFF_RECV + RECV_BYTES;
-  // full, empty, 4 more, and (CVT) "converted" and "bf16 landed" barriers per stage
-  static constexpr int OFF_MISC = OFF_BAR + ((CVT ? 4 : 2) * STAGES + 4) * 8;
+  // full, empty, 4 more, and (ACT != kActMx) "converted" and "staged part landed" per stage
+  static constexpr int OFF_MISC = OFF_BAR + ((ACT != kActMx ? 4 : 2) * STAGES + 4) * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr int TMEM_USED = BN + STAGES * SF_COLS;
   static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
@@ -214,12 +223,13 @@ __device__ __forceinline__ void epi_token_group(const KArgs& p, const float (&v)
   }
 }
 
-template <int BN, int STAGES, bool SWAP, bool CVT = false>
+template <int BN, int STAGES, bool SWAP, int ACT = kActMx>
 __global__ void __launch_bounds__(kThreads, 3)
     gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                      const KArgs p) {
-  static_assert(!CVT || (SWAP && BN == 16), "in-kernel activation quantization: decode tiles only");
-  using C = Cfg<BN, STAGES, CVT>;
+  static_assert(ACT == kActMx || (SWAP && BN == 16), "converted activations: decode tiles only");
+  constexpr bool CVT = ACT != kActMx;  // a staged activation part converted by the epilogue warps
+  using C = Cfg<BN, STAGES, ACT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sraw = smem_u32(smem_raw);
   const uint32_t sbase = (sraw + 1023u) & ~1023u;  // 128-byte-swizzled tiles need 1024-byte alignment
@@ -325,7 +335,16 @@ __global__ void __launch_bounds__(kThreads, 3)
     const uint32_t a_dst0 = sbase, b_dst0 = sbase + C::OFF_B, sf_dst0 = sbase + C::OFF_SF;
     // operand loads of k-block i into stage s; the weight operand is A in swap-AB, B otherwise
     auto load_act = [&](int s, int kb, uint32_t fb) {
-      if (SWAP && CVT) {  // bf16 activations (element coordinates) into the staging slot
+      if (SWAP && ACT == kActPackedSf) {
+        // E4M3 tile as usual; the stage's packed scale words (one per token, rows b_row0..) into
+        // the staging slot. Only rows < Mp exist in each word column of the packed array.
+        tma_load_2d(b_dst0 + s * C::B_BYTES, &tm_b, fb, static_cast<int32_t>(b_xoff + kb * BK), static_cast<int32_t>(b_row0));
+        const uint32_t ab = bar_act + (fb - bar_full);
+        const int64_t rows = p.act_mp4 - b_row0 < BN ? p.act_mp4 - b_row0 : BN;
+        mbar_arrive_expect_tx(ab, static_cast<uint32_t>(rows * 4));
+        bulk_load(sbase + C::OFF_BF + s * C::BF_BYTES, b_sf + ((b_kc0 + kb) * p.act_mp4 + b_row0) * 4,
+                  static_cast<uint32_t>(rows * 4), ab);
+      } else if (SWAP && CVT) {  // bf16 activations (element coordinates) into the staging slot
         const uint32_t ab = bar_act + (fb - bar_full);
         mbar_arrive_expect_tx(ab, C::BF_BYTES);
         tma_load_2d(sbase + C::OFF_BF + s * C::BF_BYTES, &tm_b, ab, static_cast<int32_t>(b_xoff + kb * BK),
@@ -414,7 +433,31 @@ __global__ void __launch_bounds__(kThreads, 3)
   const bool epi = warp >= 2;
   const int q = warp & 3;  // TMEM lane quarter this warp may access
   const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16);
-  if (CVT && epi) {
+  if (ACT == kActPackedSf && epi) {
+    // During the mainloop the epilogue warps move each stage's packed scale words into the
+    // F8_128x4 atom: token row r's word (its 4 group bytes) goes to bytes r * 16 .. r * 16 + 3.
+    const int t = static_cast<int>(threadIdx.x) - 64;
+    const int rows = static_cast<int>(p.act_mp4 - b_row0 < BN ? p.act_mp4 - b_row0 : BN);
+    for (int i = t; i < STAGES * 128; i += 128)  // everything else in the atoms stays zero
+      reinterpret_cast<uint32_t*>(smem + C::OFF_SF + (i >> 7) * C::SF_BYTES + 512)[i & 127] = 0u;
+    named_barrier(3, 128);
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % STAGES;
+      if (!mbar_wait_bounded(bar_act + 8 * s, (i / STAGES) & 1)) {
+        *abort_flag = 1;
+        report_timeout(p.status);
+        break;
+      }
+      if (t < rows) {
+        const uint32_t w = reinterpret_cast<const uint32_t*>(smem + C::OFF_BF + s * C::BF_BYTES)[t];
+        reinterpret_cast<uint32_t*>(smem + C::OFF_SF + s * C::SF_BYTES + 512)[t * 4] = w;
+      }
+      fence_proxy_async_smem();  // the scale copy reads the atom through the async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_conv + 8 * s);
+    }
+  }
+  if (ACT == kActBf16 && epi) {
     // During the mainloop the epilogue warps quantize each stage's bf16 activations exactly as
     // mxfp8_quantize does: thread t takes token row t / 8 and 16 elements of group (t / 2) % 4;
     // the two halves of a group meet by one shuffle for the amax.
@@ -1258,22 +1301,22 @@ int num_sms() {
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-template <int BN, int STAGES, bool CVT = false>
+template <int BN, int STAGES, int ACT = kActMx>
 int ctas_per_sm() {
-  using C = Cfg<BN, STAGES, CVT>;
+  using C = Cfg<BN, STAGES, ACT>;
   const int by_smem = C::SM_SMEM / (C::SMEM_LAUNCH + 1024);
   const int by_tmem = 512 / C::TMEM_COLS;
   return by_smem < by_tmem ? by_smem : by_tmem;
 }
 
-template <int BN, int STAGES, bool SWAP, bool CVT = false>
+template <int BN, int STAGES, bool SWAP, int ACT = kActMx>
 cudaError_t launch_cfg(const GemmLaunch& l, const KArgs& ka, dim3 grid, int cluster_z, cudaStream_t stream) {
-  using C = Cfg<BN, STAGES, CVT>;
-  auto kern = gemm_mxf8_kernel<BN, STAGES, SWAP, CVT>;
+  using C = Cfg<BN, STAGES, ACT>;
+  auto kern = gemm_mxf8_kernel<BN, STAGES, SWAP, ACT>;
   static const cudaError_t attr_err = set_smem_attrs(kern, C::SMEM_LAUNCH);
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap tma_act, tma_wt;
-  if (CVT) {
+  if (ACT == kActBf16) {
     if (!make_bf16_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, BN)) return cudaErrorInvalidValue;
   } else if (!make_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, SWAP ? BN : BM)) {
     return cudaErrorInvalidValue;
@@ -1307,26 +1350,26 @@ cudaError_t launch_cfg(const GemmLaunch& l, const KArgs& ka, dim3 grid, int clus
 // Largest split of the K range (cluster size) that divides the k-blocks, leaves every rank at
 // least 4 token columns, fits its staging in shared memory and keeps every CTA resident in one
 // wave.
-template <int BN, int STAGES, bool CVT = false>
+template <int BN, int STAGES, int ACT = kActMx>
 int pick_splits(int tiles, int kb_total, int slots) {
   for (int s = 8; s > 1; s >>= 1)
-    if (kb_total % s == 0 && BN / s >= 4 && Cfg<BN, STAGES, CVT>::split_fits(s) && tiles * s <= slots) return s;
+    if (kb_total % s == 0 && BN / s >= 4 && Cfg<BN, STAGES, ACT>::split_fits(s) && tiles * s <= slots) return s;
   return 1;
 }
 
-template <int BN, int STAGES, bool CVT = false>
+template <int BN, int STAGES, int ACT = kActMx>
 cudaError_t launch_swap(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   const int tok_tiles = static_cast<int>(ceil_div(l.T, BN));
   const int tiles = l.G * (l.n_feat / BM) * tok_tiles;
   const int kb_total = l.k_len / BK;
-  const int slots = num_sms() * ctas_per_sm<BN, STAGES, CVT>();
-  const int s = pick_splits<BN, STAGES, CVT>(tiles, kb_total, slots);
+  const int slots = num_sms() * ctas_per_sm<BN, STAGES, ACT>();
+  const int s = pick_splits<BN, STAGES, ACT>(tiles, kb_total, slots);
   ka.splits = s;
   ka.kb_per_cta = kb_total / s;
   ka.per_rank_shift = 0;
   while ((1 << ka.per_rank_shift) < BN / s) ++ka.per_rank_shift;
   dim3 grid(static_cast<unsigned>(l.n_feat / BM), static_cast<unsigned>(tok_tiles), static_cast<unsigned>(l.G * s));
-  return launch_cfg<BN, STAGES, true, CVT>(l, ka, grid, s, stream);
+  return launch_cfg<BN, STAGES, true, ACT>(l, ka, grid, s, stream);
 }
 
 template <int BN, int STAGES>
@@ -1433,6 +1476,7 @@ cudaError_t launch_gemm(const GemmLaunch& l, cudaStream_t stream) {
   ka.z_mp4 = ceil_div(l.T, 4) * 4;
   ka.status = l.status;
   ka.pdl = l.pdl ? 1 : 0;
+  ka.act_mp4 = ceil_div(l.T, 4) * 4;
   if (l.n_feat % BM != 0 || l.k_len % BK != 0) return cudaErrorInvalidValue;
   // swap-AB (weights on the MMA's M side) while the token count is small: one token tile of
   // N = 16..128, or several 128-token tiles
@@ -1441,7 +1485,12 @@ cudaError_t launch_gemm(const GemmLaunch& l, cudaStream_t stream) {
   // grids keep 5 stages, about 14 MB of loads in flight
   if (l.act_is_bf16) {  // bf16 activations, quantized in the kernel: decode tiles only
     if (l.T > 16) return cudaErrorInvalidValue;
-    return launch_swap<16, 3, true>(l, ka, stream);
+    return launch_swap<16, 3, kActBf16>(l, ka, stream);
+  }
+  if (l.act_sf_packed) {  // int32-packed activation scales, moved into atoms in the kernel
+    if (l.T > 16) return cudaErrorInvalidValue;
+    return l.has_dependent ? launch_swap<16, 3, kActPackedSf>(l, ka, stream)
+                           : launch_swap<16, 5, kActPackedSf>(l, ka, stream);
   }
   if (l.T <= 16) return l.has_dependent ? launch_swap<16, 3>(l, ka, stream) : launch_swap<16, 5>(l, ka, stream);
   if (l.T <= 32) return launch_swap<32, 5>(l, ka, stream);

@@ -65,6 +65,8 @@ struct GemmLaunch {
   // act is bf16 [T, act_cols] (row stride act_ld elements), quantized to MXFP8 inside the
   // kernel with mxfp8_quantize's rule; act_sf is unused. T <= 16 only.
   bool act_is_bf16;
+  // act_sf is MXQ_SF_PACKED_I32_MN (packed[w * Mp + m], Mp = ceil(T / 4) * 4). T <= 16 only.
+  bool act_sf_packed;
 };
 cudaError_t launch_gemm(const GemmLaunch& a, cudaStream_t stream);
 

@@ -314,6 +314,35 @@ def test_o_proj_from_bf16_matches_prequantized(mxq, weights, T, pad):
         assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("T", [1, 5, 16])
+def test_wo_b_reads_packed_scales(mxq, weights, T):
+    """wo_b taking z with int32-packed MN-major scales (the layout the fused epilogue writes as
+    its second output) gives the same bf16 output as with the F8_128x4 scales, standalone and as
+    the dependent half of the pair."""
+    from mxfp8_activation_quant_gb300 import synth
+
+    O = gpu_mx(mxq, synth.o_proj_activation(9, T))
+    zq = torch.empty((T, synth.KB), dtype=torch.uint8, device="cuda")
+    ztl, zpk = mxq.empty_sf(2, T, synth.KB), mxq.empty_sf(1, T, synth.KB)
+    out = torch.empty((T, synth.NB), dtype=torch.bfloat16, device="cuda")
+    mxq.o_proj_mxfp8(O, weights.WA, weights.WB, T, synth.G, synth.NA, synth.KA, synth.NB, zq, ztl, out,
+                     z_sf_packed=zpk)
+    out_pk = torch.empty_like(out)
+    mxq.gemm_mxfp8_bf16(mxq.MXFP8(zq, zpk, mxq.SF_PACKED_I32_MN), weights.WB, out_pk)
+    out_tl = torch.empty_like(out)
+    mxq.gemm_mxfp8_bf16(mxq.MXFP8(zq, ztl), weights.WB, out_tl)
+    torch.cuda.synchronize()
+    assert torch.equal(out_pk, out_tl)
+    # the standalone wo_b (5 stages) splits K like the paired one: same bytes as the pair too
+    assert torch.equal(out_pk, out)
+    if T == 16:
+        big = mxq.MXFP8(torch.zeros((17, synth.KB), dtype=torch.uint8, device="cuda"),
+                        mxq.empty_sf(1, 17, synth.KB), mxq.SF_PACKED_I32_MN)
+        with pytest.raises(mxq.MxqError) as e:
+            mxq.gemm_mxfp8_bf16(big, weights.WB, torch.empty((17, synth.NB), dtype=torch.bfloat16, device="cuda"))
+        assert e.value.status == 2
+
+
 def test_status_word_stays_clear(mxq, weights):
     from mxfp8_activation_quant_gb300 import synth
 
