@@ -712,214 +712,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
 }
 
-// ------------------------------------------------------------------------------------------
-// Persistent normal-orientation kernel (large T). One CTA per SM walks the tiles
-// t = blockIdx.x, blockIdx.x + gridDim.x, ... (feature tiles fastest). The producer streams
-// k-blocks across tile boundaries, so the next tile's operands arrive while the current
-// tile's epilogue runs. Eight epilogue warps each copy 128 accumulator columns of their
-// TMEM lane quarter into registers and immediately hand the accumulator back to the MMA
-// warp (barrier `acc_empty`), so the next tile's MMAs overlap the conversion and stores.
-// ------------------------------------------------------------------------------------------
-constexpr int kThreadsP = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
-
-template <int BN, int STAGES>
-__global__ void __launch_bounds__(kThreadsP, 1)
-    gemm_mxf8_persistent(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                         const KArgs p) {
-  using C = Cfg<BN, STAGES>;
-  static_assert(BN == 256, "epilogue splits the accumulator into two 128-column halves");
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t sraw = smem_u32(smem_raw);
-  const uint32_t sbase = (sraw + 1023u) & ~1023u;
-  uint8_t* smem = smem_raw + (sbase - sraw);
-  const uint32_t bar_full = sbase + C::OFF_BAR;
-  const uint32_t bar_empty = bar_full + STAGES * 8;
-  const uint32_t bar_accf = bar_empty + STAGES * 8;  // accumulator full (MMA -> epilogue)
-  const uint32_t bar_acce = bar_accf + 8;            // accumulator empty (epilogue -> MMA)
-  const uint32_t bar_drain = bar_accf + 16;          // abort path: all tcgen05 ops completed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  int* issued_cnt = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
-  int* consumed_cnt = reinterpret_cast<int*>(smem + C::OFF_MISC + 12);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  const int n_tiles = p.n_feat / BN;
-  const int m_tiles = static_cast<int>((p.T + BM - 1) / BM);
-  const int per_group = m_tiles * n_tiles;
-  const int total = per_group * p.G;
-  const int nk = p.kb_per_cta;
-  // tile -> (group, token tile, feature tile)
-  auto decode = [&](int t, int& g, int64_t& m0, int64_t& n0) {
-    g = t / per_group;
-    const int r = t - g * per_group;
-    m0 = static_cast<int64_t>(r / n_tiles) * BM;
-    n0 = static_cast<int64_t>(r % n_tiles) * BN;
-  };
-
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_a);
-    tma_prefetch_desc(&tm_b);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
-    }
-    mbar_init(bar_accf, 1);
-    mbar_init(bar_acce, 8);  // one arrival per epilogue warp
-    mbar_init(bar_drain, 1);
-    *abort_flag = 0;
-    *issued_cnt = 0;
-    *consumed_cnt = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0 && lane == 0) {
-    // ---------------- producer ----------------
-    int it = 0;
-    bool first = true;
-    for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-      int g;
-      int64_t m0, n0;
-      decode(t, g, m0, n0);
-      const int64_t a_x = static_cast<int64_t>(g) * p.act_k_per_group;
-      const int64_t a_rt = m0 >> 7, a_kc0 = a_x >> 7;
-      const int64_t b_row = static_cast<int64_t>(g) * p.n_feat + n0, b_rt0 = b_row >> 7;
-      auto load_act = [&](int s, int kb, uint32_t fb) {
-        tma_load_2d(sbase + s * C::A_BYTES, &tm_a, fb, static_cast<int32_t>(a_x + kb * BK), static_cast<int32_t>(m0));
-        bulk_load(sbase + C::OFF_SF + s * C::SF_BYTES, p.act_sf + (a_rt * p.act_gp4 + a_kc0 + kb) * 512, 512, fb);
-      };
-      auto load_wt = [&](int s, int kb, uint32_t fb) {
-        tma_load_2d(sbase + C::OFF_B + s * C::B_BYTES, &tm_b, fb, static_cast<int32_t>(kb * BK), static_cast<int32_t>(b_row));
-#pragma unroll
-        for (int j = 0; j < C::SFB_ATOMS; ++j)
-          bulk_load(sbase + C::OFF_SF + s * C::SF_BYTES + 512 * (1 + j), p.wt_sf + ((b_rt0 + j) * p.wt_gp4 + kb) * 512,
-                    512, fb);
-      };
-      int kb = 0;
-      if (first && p.pdl) {
-        // weights of the first stages before waiting for the grid that produces the activations
-        const int pre = nk < STAGES ? nk : STAGES;
-        for (int j = 0; j < pre; ++j) {
-          mbar_arrive_expect_tx(bar_full + 8 * j, C::TX_BYTES);
-          load_wt(j, j, bar_full + 8 * j);
-        }
-        pdl_wait_primary();
-        for (int j = 0; j < pre; ++j) load_act(j, j, bar_full + 8 * j);
-        kb = pre;
-        it = pre;
-      }
-      first = false;
-      for (; kb < nk; ++kb, ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        if (!mbar_wait_bounded(bar_empty + 8 * s, ph ^ 1)) {
-          *abort_flag = 1;
-          report_timeout(p.status);
-          break;
-        }
-        const uint32_t fb = bar_full + 8 * s;
-        mbar_arrive_expect_tx(fb, C::TX_BYTES);
-        load_wt(s, kb, fb);
-        load_act(s, kb, fb);
-      }
-    }
-    *issued_cnt = it;
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer ----------------
-    int it = 0, ti = 0;
-    for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++ti) {
-      if (!mbar_wait_bounded(bar_acce, (ti & 1) ^ 1)) {  // accumulator drained by the epilogue
-        *abort_flag = 1;
-        report_timeout(p.status);
-        break;
-      }
-      tc_fence_after();
-      bool ok = true;
-      for (int kb = 0; kb < nk; ++kb, ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        if (!mbar_wait_bounded(bar_full + 8 * s, ph)) {
-          *abort_flag = 1;
-          report_timeout(p.status);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t sf_src = sbase + C::OFF_SF + s * C::SF_BYTES;
-        const uint32_t sfa_t = tmem + BN + s * C::SF_COLS;
-        const uint32_t sfb_t = sfa_t + 4;
-        tc_cp_sf_atom(sfa_t, sdesc_sf_atom(sf_src));
-#pragma unroll
-        for (int j = 0; j < C::SFB_ATOMS; ++j) tc_cp_sf_atom(sfb_t + 4 * j, sdesc_sf_atom(sf_src + 512 * (1 + j)));
-        const uint64_t ad = sdesc_kmajor_sw128(sbase + s * C::A_BYTES);
-        const uint64_t bd = sdesc_kmajor_sw128(sbase + C::OFF_B + s * C::B_BYTES);
-#pragma unroll
-        for (int k = 0; k < BK / 32; ++k)
-          tc_mma_mxf8(tmem, ad + 2 * k, bd + 2 * k, idesc_mxf8(BM, BN, k, k), sfa_t, sfb_t, (kb | k) != 0 ? 1u : 0u);
-        tc_commit(bar_empty + 8 * s);
-      }
-      tc_commit(bar_accf);
-      if (!ok) break;
-    }
-    *consumed_cnt = it;
-    pdl_launch_dependents();  // every tile of this CTA has been issued
-  } else if (warp >= 2) {
-    // ---------------- epilogue ----------------
-    const int q = warp & 3;          // TMEM lane quarter
-    const int half = (warp - 2) >> 2;  // accumulator columns [128*half, 128*half + 128)
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16) + 128 * half;
-    int ti = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++ti) {
-      if (!mbar_wait_bounded(bar_accf, ti & 1)) {
-        *abort_flag = 1;
-        report_timeout(p.status);
-      }
-      if (__any_sync(0xffffffffu, *abort_flag)) break;
-      tc_fence_after();
-      uint32_t acc[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_x32(t_lane + 32 * c, acc[c]);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_acce);  // the MMA warp may overwrite the accumulator now
-      int g;
-      int64_t m0, n0;
-      decode(t, g, m0, n0);
-      const int64_t row = m0 + 32 * q + lane;
-      const int64_t col0 = static_cast<int64_t>(g) * p.n_feat + n0 + 128 * half;
-      uint32_t word = 0;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) epi_row_chunk(p, acc[c], row, col0 + 32 * c, word, c);
-    }
-  }
-  __syncwarp();
-
-  tc_fence_before();
-  __syncthreads();
-  if (*abort_flag) {
-    if (warp == 0 && lane == 0) {
-      for (int i = *consumed_cnt; i < *issued_cnt; ++i)
-        (void)mbar_wait_bounded(bar_full + 8 * (i % STAGES), (i / STAGES) & 1);
-    }
-    if (warp == 1 && lane == 0) {
-      tc_commit(bar_drain);  // arrives once every MMA / copy this thread issued has completed
-      (void)mbar_wait_bounded(bar_drain, 0);
-    }
-    __syncthreads();
-  }
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
-  }
-}
+constexpr int kThreadsP = 320;  // the pair kernel's warps 0..9 (warp 10 is added below)
 
 // ------------------------------------------------------------------------------------------
 // CTA-pair persistent kernel (large T). One tcgen05 MMA of M = 256 tokens x N = 256 features
@@ -928,7 +721,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 // a 128 x 256 tile on one SM, for the same tensor work per SM. Both CTAs' loads complete on the
 // even CTA's stage barriers; the even CTA's MMA warp issues the MMAs, and their commits arrive
 // on both CTAs' barriers. Each CTA drains its half of the accumulator (its 128 token rows x 256
-// columns, in its own TMEM) exactly as gemm_mxf8_persistent does.
+// columns, in its own TMEM) with four tcgen05.ld and releases it at once.
 // ------------------------------------------------------------------------------------------
 template <int STAGES>
 struct PairCfg {
@@ -1379,36 +1172,6 @@ cudaError_t launch_normal(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   dim3 grid(static_cast<unsigned>(l.n_feat / BN), static_cast<unsigned>(ceil_div(l.T, BM)),
             static_cast<unsigned>(l.G));
   return launch_cfg<BN, STAGES, false>(l, ka, grid, 1, stream);
-}
-
-// persistent normal-orientation launch: one CTA per SM (or fewer when there are fewer tiles)
-template <int BN, int STAGES>
-cudaError_t launch_persistent(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
-  using C = Cfg<BN, STAGES>;
-  auto kern = gemm_mxf8_persistent<BN, STAGES>;
-  static const cudaError_t attr_err = set_smem_attrs(kern, C::SMEM_LAUNCH);
-  if (attr_err != cudaSuccess) return attr_err;
-  ka.splits = 1;
-  ka.kb_per_cta = l.k_len / BK;
-  const int64_t tiles = static_cast<int64_t>(l.G) * ceil_div(l.T, BM) * (l.n_feat / BN);
-  const int ctas = static_cast<int>(tiles < num_sms() ? tiles : num_sms());
-  CUtensorMap tma_act, tma_wt;
-  if (!make_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, BM)) return cudaErrorInvalidValue;
-  if (!make_map(&tma_wt, l.wt, static_cast<int64_t>(l.G) * l.n_feat, l.k_len, l.wt_ld, BN)) return cudaErrorInvalidValue;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
-  cfg.blockDim = dim3(kThreadsP, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM_LAUNCH;
-  cfg.stream = stream;
-  cudaLaunchAttribute attrs[1];
-  cfg.numAttrs = 0;
-  if (ka.pdl) {
-    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attrs[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.numAttrs = 1;
-  }
-  cfg.attrs = attrs;
-  return cudaLaunchKernelEx(&cfg, kern, tma_act, tma_wt, ka);
 }
 
 }  // namespace
