@@ -190,6 +190,15 @@ MXQ_API mxq_status o_proj_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa,
                                 void* status, void* stream);
 
 /*
+ * mxq_selftest_wait_timeout -- exercises the failure path every kernel shares: one thread waits
+ * with the pipelines' bounded mbarrier wait (here limited to limit_us microseconds, 1..10^6) on a
+ * barrier nothing arrives on, gives up, and records MXQ_ERR_TIMEOUT in the status word, which
+ * mxq_check_status then returns. The context stays usable. No page describes it; it is a
+ * diagnostic of this library. status: a zeroed status word (required).
+ */
+MXQ_API mxq_status mxq_selftest_wait_timeout(int64_t limit_us, void* status, void* stream);
+
+/*
  * o_proj_mxfp8_from_bf16 -- the _o_proj pair at decode sizes (T <= 16) fed by bf16 o
  * ([KeepMXFP8] Pieces: the small-M wo_a that quantizes its activation in the kernel, "pre-quantized
  * == in-kernel"). wo_a loads o as bf16 and quantizes each tile in shared memory with exactly the

@@ -53,6 +53,7 @@ SIGNATURES = {
     "mxq_sf_bytes": ([I32, I64, I64], ctypes.c_size_t),
     "mxq_status_bytes": ([], ctypes.c_size_t),
     "mxq_check_status": ([P, P], ctypes.c_int),
+    "mxq_selftest_wait_timeout": ([I64, P, P], ctypes.c_int),
     "mxfp8_quantize": ([P, I64, I64, I64, P, I64, P, P, P, P], ctypes.c_int),
     "rmsnorm_dual_out": ([P, P, ctypes.c_float, I64, I64, I64, P, P, P, P, P, P], ctypes.c_int),
     "wo_a_einsum_mxfp8": ([_MXP, _MXP, I64, I32, I32, I32, P, P, P, P, P, P], ctypes.c_int),
@@ -216,3 +217,8 @@ def o_proj_mxfp8_from_bf16(o: torch.Tensor, wa: MXFP8, wb: MXFP8, T: int, G: int
     _check(load().o_proj_mxfp8_from_bf16(_ptr(o), o.stride(0), ctypes.byref(ac), ctypes.byref(bc), T, G, Na, Ka, Nb,
                                          _ptr(z_q), _ptr(z_sf_128x4), _ptr(z_sf_packed), _ptr(z_bf16), _ptr(out),
                                          _ptr(status), _stream(stream)), "o_proj_mxfp8_from_bf16")
+
+
+def selftest_wait_timeout(limit_us: int, status: torch.Tensor, stream=None) -> None:
+    """Launch the bounded-wait self-test: a wait that runs out after limit_us and reports a timeout."""
+    _check(load().mxq_selftest_wait_timeout(limit_us, _ptr(status), _stream(stream)), "mxq_selftest_wait_timeout")

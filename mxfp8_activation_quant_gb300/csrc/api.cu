@@ -6,10 +6,24 @@
 #include <cstring>
 
 #include "mxq.h"
+#include "mxq_device.cuh"
 #include "mxq_internal.h"
 
 namespace {
 thread_local char g_last_error[128] = "no error";
+
+// An mbarrier that nothing will ever arrive on, waited on with the pipelines' own bounded wait
+// (a shorter limit): the wait runs out and the timeout is reported the way every kernel reports
+// it. Nothing faults and nothing hangs.
+__global__ void selftest_wait_kernel(uint64_t limit_ns, int32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = mxq::smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mxq::mbar_init(b, 1);
+    mxq::fence_mbar_init();
+    if (!mxq::mbar_wait_limit(b, 0, limit_ns) && status != nullptr) atomicCAS(status, 0, MXQ_ERR_TIMEOUT);
+  }
+}
 }  // namespace
 
 mxq_status mxq::from_cuda(cudaError_t e) {
@@ -276,6 +290,14 @@ mxq_status o_proj_mxfp8_from_bf16(const void* o_bf16, int64_t ld_o, const mxq_mx
   if (st != MXQ_OK) return st;
   const mxq_mx_tensor z = {z_q, z_sf_128x4, MXQ_SF_TILED_128X4, T, Kb, Kb};
   return gemm_impl(&z, wb, T, Nb, Kb, out_bf16, Nb, status, stream, true);
+}
+
+mxq_status mxq_selftest_wait_timeout(int64_t limit_us, void* status, void* stream) {
+  if (status == nullptr || limit_us < 1 || limit_us > 1000000) return MXQ_ERR_INVALID_ARG;
+  if (!al16(status)) return MXQ_ERR_MISALIGNED;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint64_t>(limit_us) * 1000u,
+                                                                      static_cast<int32_t*>(status));
+  return from_cuda(cudaGetLastError());
 }
 
 }  // extern "C"

@@ -27,7 +27,7 @@ def test_every_declared_symbol_is_exported(lib):
     from mxfp8_activation_quant_gb300 import _lib
 
     names = declared_functions()
-    assert len(names) == 13, names
+    assert len(names) == 14, names
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(_lib.SIGNATURES)
@@ -132,3 +132,10 @@ def test_o_proj_from_bf16_argument_errors(lib):
     assert f(FAKE, 32000, *args, 4, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, None, None) == 2  # ld_o
     assert f(FAKE + 2, 32768, *args, 4, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, None, None) == 3
     assert f(FAKE, 32772, *args, 4, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, None, None) == 3  # ld_o*2 % 16
+
+
+def test_selftest_argument_errors(lib):
+    assert lib.mxq_selftest_wait_timeout(1000, None, None) == 1
+    assert lib.mxq_selftest_wait_timeout(0, FAKE, None) == 1
+    assert lib.mxq_selftest_wait_timeout(2000000, FAKE, None) == 1  # the limit stays within 1 s
+    assert lib.mxq_selftest_wait_timeout(1000, FAKE + 4, None) == 3
