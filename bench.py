@@ -371,7 +371,8 @@ def traffic_for(kernel, T):
 def sweep(args, mxq, synth, torch, dev, WA, WB):
     """Per-config lines for the sweep tables (not the headline line): quantizer, RMSNorm, and
     the _o_proj pair fused vs unfused (wo_a bf16 z -> standalone quantize -> wo_b), timed under
-    CUDA-graph replay with a cold L2 (the pages' method: "full CUDA graph, cold L2")."""
+    CUDA-graph replay with a cold L2 (how the pages time the pair: the whole call captured in a
+    CUDA graph, L2 flushed before it)."""
     hbm, bf16_tf, _ = load_peaks()
     mx_tf = 2 * bf16_tf
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size

@@ -7,7 +7,7 @@
  *
  * MXFP8 here means: E4M3 values (OCP FP8, "FN" variant, largest finite 448) with one UE8M0
  * scale byte b (value 2^(b-127)) per 32 consecutive elements along the contraction / row
- * dimension K ([KeepMXFP8] review: "1 scale per 32 elements along K"). For a group with
+ * dimension K (the [KeepMXFP8] review fixes one scale for each 32 elements along K). For a group with
  * largest magnitude amax the scale 2^e is the smallest power of two with amax / 2^e <= 448
  * (never below 2^-127; an all-zero group takes byte 0), and each element x is stored as the
  * E4M3 value nearest to x * 2^-e (round to nearest, ties to even, saturating at +-448; the
@@ -143,7 +143,7 @@ MXQ_API mxq_status rmsnorm_dual_out(const void* x_bf16, const void* gamma_bf16, 
 
 /*
  * wo_a_einsum_mxfp8 -- the grouped wo_a einsum of DeepSeek-V4.1's _o_proj ([MegaAttn]
- * Validation: "8 groups x 4096 -> 1024"), read as tgk,gnk->tgn:
+ * Validation: 8 groups, 4096 in, 1024 out), read as tgk,gnk->tgn:
  *   z[t, g*Na + n] = sum_k deq(o)[t, g*Ka + k] * deq(wa)[g*Na + n, k]   (fp32 accumulation)
  * with the fused epilogue of [MegaAttn] Overview/Details: the fp32 result is rounded to bf16
  * and that bf16 z is quantized to MXFP8 in registers (scales in F8_128x4), so no standalone
@@ -164,7 +164,7 @@ MXQ_API mxq_status wo_a_einsum_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor
 
 /*
  * gemm_mxfp8_bf16 -- the wo_b MXFP8 GEMM ([MegaAttn] Validation: "wo_b 8192 -> 5120"; it
- * "takes the QuantizedActivation directly"):
+ * consumes the quantized activation as it is):
  *   out[m, n] = RNE_bf16( sum_k deq(a)[m, k] * deq(b)[n, k] )   (fp32 accumulation)
  *   a : [M, K] MXFP8 activations, b : [N, K] MXFP8 weights, both MXQ_SF_TILED_128X4; for
  *       M <= 16 the activation scales may also be MXQ_SF_PACKED_I32_MN ([KeepMXFP8] Pieces: the

@@ -1,7 +1,7 @@
 // Block-scaled MXFP8 GEMMs of the _o_proj chain on 5th-generation tensor cores (sm_103a).
 //
 // Pages: "[Perf][DSv4.1] MegaAttn: wo_a writes wo_b's MXFP8 input" (Overview, Validation,
-// Details): wo_a is a grouped FP8 einsum "8 groups x 4096 -> 1024" whose epilogue writes z as
+// Details): wo_a is a grouped FP8 einsum (8 groups, 4096 in, 1024 out) whose epilogue writes z as
 // MXFP8 with F8_128x4 scales; wo_b is an MXFP8 GEMM "8192 -> 5120" that takes that z directly.
 //
 // One kernel template serves both. Per CTA (192 threads):

@@ -2,7 +2,7 @@
 //
 // Quantizer: page "[Perf][DSv4.1] MegaAttn: wo_a writes wo_b's MXFP8 input" (Claims: the
 // standalone mxfp8_quantize launch) and "[Perf][DSv4.1] Keep activations MXFP8 between
-// DeepGEMM kernels" (Purpose: the "[q]" launch, "1 scale per 32 elements along K").
+// DeepGEMM kernels" (Purpose: the "[q]" launch; one scale for each 32 elements along K).
 // RMSNorm: the latter page's "mega_mhc (post+pre+RMSNorm)" producer emitting bf16 and
 // "(y_fp8, y_gemm_sf)" in one kernel (RMSNorm part only).
 //

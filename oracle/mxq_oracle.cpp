@@ -9,7 +9,7 @@
 //        sections Overview, Claims, Validation, Details.
 //   [P4] "[Perf][DSv4.1] Keep activations MXFP8 between DeepGEMM kernels" (vllm#57977),
 //        section Purpose (before/after diagrams, per-layer table, Pieces) and the review's
-//        "1 scale per 32 elements along K".
+//        one scale for each 32 elements along K.
 // The pages name MXFP8 (OCP FP8 E4M3 values + UE8M0 power-of-two scales per 32 elements) but
 // do not define it; every reading taken where they are silent is listed at its function.
 //
@@ -159,7 +159,7 @@ void orc_ue8m0_from_amax(const double* amax, int64_t n, uint8_t* out) {
 
 // ---- group quantizer ----------------------------------------------------------------------
 // x: bf16 [M, K] with row stride ldx elements; K % 32 == 0. Groups are 32 consecutive
-// elements along K ("1 scale per 32 elements along K"). For each group: amax = max |x_i|,
+// elements along K (one scale for each 32 elements, per the review). For each group: amax = max |x_i|,
 // byte b = ue8m0_from_amax(amax), e = b - 127, q_i = E4M3(x_i * 2^-e).
 // Outputs q [M, K] (row stride K) and row-major scales sf [M, K/32].
 void orc_quantize_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
@@ -252,7 +252,7 @@ void orc_gemm_nt(const double* A, const double* B, int64_t M, int64_t N, int64_t
     }
 }
 
-// The wo_a grouped einsum "8 groups x 4096 -> 1024" read as tgk,gnk->tgn:
+// The wo_a grouped einsum (8 groups, 4096 in, 1024 out) read as tgk,gnk->tgn:
 //   z[t, g*Na + n] = sum_k o[t, g*Ka + k] * wa[g*Na + n, k]
 // o: [T, G*Ka]; wa: [G*Na, Ka]; z: [T, G*Na] (g-major flattening of [T, G, Na]).
 void orc_einsum_wo_a(const double* o, const double* wa, int64_t T, int64_t G, int64_t Na, int64_t Ka,

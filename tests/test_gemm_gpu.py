@@ -6,7 +6,7 @@ Overview / Validation / Details).
     scale-layout or descriptor error);
   * wo_a bf16 z within 4e-3 relative Frobenius of the fp64 oracle; the fused MXFP8 z bytes and
     scales identical to the standalone quantizer applied to the same call's bf16 z (the pages'
-    "wo_b receives byte-identical FP8 data and scales");
+    claim that wo_b gets the very same FP8 bytes and scales as before the fusion);
   * the whole _o_proj output within 1e-2 relative Frobenius of the oracle's own chain.
 Token counts follow the pages' tests: 1, 129, 8193 tokens and M in {1, 4, 7, 64, 300}, plus the
 decode and prefill sweeps."""

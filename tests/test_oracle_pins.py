@@ -7,7 +7,7 @@ torch's rms_norm, closed forms and invariants.
 
 Format facts pinned here come from the OCP FP8 E4M3 definition that the pages name as
 "MXFP8 / OCP FP8" (page "[Perf][DSv4.1] Keep activations MXFP8 between DeepGEMM kernels",
-review) and from the scale rule "smallest power of two 2^e with amax / 2^e <= 448".
+review) and from the scale rule: the smallest power of two 2^e with amax / 2^e <= 448.
 """
 import json
 import os
