@@ -47,6 +47,7 @@ struct KArgs {
   int32_t kb_per_cta;       // 128-wide k-blocks per CTA
   int32_t splits;           // swap-AB: CTAs per cluster along K
   int32_t pdl;              // launched as a programmatic dependent: prefetch weights, then wait
+  int32_t early;            // issue the first stages during setup (never with pdl)
   int32_t per_rank_shift;   // log2(reduction columns owned by each cluster rank)
   int64_t act_k_per_group;  // activation column offset between groups
   const uint8_t* act_sf;
@@ -189,6 +190,35 @@ __device__ __forceinline__ void epi_zero_scale(const KArgs& p, int64_t t, int64_
   if (p.z_sf_pk != nullptr && t < p.z_mp4) p.z_sf_pk[((gi >> 2) * p.z_mp4 + t) * 4 + (gi & 3)] = 0;
 }
 
+// swap orientation, split-K decode tiles: one warp finishes one 32-feature group of four
+// consecutive tokens t0..t0+3. Lane l holds the fp32 sums of feature col + l for the four
+// tokens (x, y, z, w); the group amax is one warp reduction per token.
+__device__ __forceinline__ void epi_group_tokens4(const KArgs& p, const float4 s, int64_t t0, int64_t col, int lane) {
+  const uint32_t h01 = bf16x2_rn(s.x, s.y), h23 = bf16x2_rn(s.z, s.w);
+  const uint32_t hv[4] = {h01 & 0xFFFFu, h01 >> 16, h23 & 0xFFFFu, h23 >> 16};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int64_t t = t0 + k;  // the same in every lane
+    if (t >= p.z_mp128) break;
+    if (t >= p.T) {  // padding token: only its zero scale is stored
+      if (lane == 0) epi_zero_scale(p, t, col);
+      continue;
+    }
+    if (p.out_bf16 != nullptr) p.out_bf16[t * p.ldo + col + lane] = static_cast<uint16_t>(hv[k]);
+    if (p.z_q != nullptr) {
+      const uint32_t code = ue8m0_from_bf16_amax(__reduce_max_sync(0xffffffffu, hv[k] & 0x7FFFu));
+      p.z_q[t * p.ldz + col + lane] = static_cast<uint8_t>(e4m3x2(bf16_lo(hv[k]) * ue8m0_inverse(code), 0.f));
+      if (lane == 0) {
+        const int64_t gi = col >> 5;
+        if (p.z_sf_tl != nullptr)
+          p.z_sf_tl[tiled128x4_word_offset(t, gi >> 2, p.z_gp4) + (gi & 3)] = static_cast<uint8_t>(code);
+        if (p.z_sf_pk != nullptr && t < p.z_mp4)
+          p.z_sf_pk[((gi >> 2) * p.z_mp4 + t) * 4 + (gi & 3)] = static_cast<uint8_t>(code);
+      }
+    }
+  }
+}
+
 // swap orientation, after the partial sums are in shared memory: one thread = one token and
 // one 32-feature quantization group. v[0..31] are the fp32 sums for features col..col+31 of
 // token t (col = first output column of the group).
@@ -288,7 +318,46 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
   const int kb_begin = split * p.kb_per_cta;
   const int nk = p.kb_per_cta;
+  const int pre = nk < STAGES ? nk : STAGES;  // stages that need no free-slot wait
 
+  const uint32_t a_dst0 = sbase, b_dst0 = sbase + C::OFF_B, sf_dst0 = sbase + C::OFF_SF;
+  // operand loads of k-block i into stage s; the weight operand is A in swap-AB, B otherwise
+  auto load_act = [&](int s, int kb, uint32_t fb) {
+    if (SWAP && ACT == kActPackedSf) {
+      // E4M3 tile as usual; the stage's packed scale words (one per token, rows b_row0..) into
+      // the staging slot. Only rows < Mp exist in each word column of the packed array.
+      tma_load_2d(b_dst0 + s * C::B_BYTES, &tm_b, fb, static_cast<int32_t>(b_xoff + kb * BK), static_cast<int32_t>(b_row0));
+      const uint32_t ab = bar_act + (fb - bar_full);
+      const int64_t rows = p.act_mp4 - b_row0 < BN ? p.act_mp4 - b_row0 : BN;
+      mbar_arrive_expect_tx(ab, static_cast<uint32_t>(rows * 4));
+      bulk_load(sbase + C::OFF_BF + s * C::BF_BYTES, b_sf + ((b_kc0 + kb) * p.act_mp4 + b_row0) * 4,
+                static_cast<uint32_t>(rows * 4), ab);
+    } else if (SWAP && CVT) {  // bf16 activations (element coordinates) into the staging slot
+      const uint32_t ab = bar_act + (fb - bar_full);
+      mbar_arrive_expect_tx(ab, C::BF_BYTES);
+      tma_load_2d(sbase + C::OFF_BF + s * C::BF_BYTES, &tm_b, ab, static_cast<int32_t>(b_xoff + kb * BK),
+                  static_cast<int32_t>(b_row0));
+    } else if (SWAP) {
+      tma_load_2d(b_dst0 + s * C::B_BYTES, &tm_b, fb, static_cast<int32_t>(b_xoff + kb * BK), static_cast<int32_t>(b_row0));
+#pragma unroll
+      for (int j = 0; j < C::SFB_ATOMS; ++j)
+        bulk_load(sf_dst0 + s * C::SF_BYTES + 512 * (1 + j), b_sf + ((b_rt0 + j) * b_gp4 + b_kc0 + kb) * 512, 512, fb);
+    } else {
+      tma_load_2d(a_dst0 + s * C::A_BYTES, &tm_a, fb, static_cast<int32_t>(a_xoff + kb * BK), static_cast<int32_t>(a_row0));
+      bulk_load(sf_dst0 + s * C::SF_BYTES, a_sf + (a_rt * a_gp4 + a_kc0 + kb) * 512, 512, fb);
+    }
+  };
+  auto load_wt = [&](int s, int kb, uint32_t fb) {
+    if (SWAP) {
+      tma_load_2d(a_dst0 + s * C::A_BYTES, &tm_a, fb, static_cast<int32_t>(a_xoff + kb * BK), static_cast<int32_t>(a_row0));
+      bulk_load(sf_dst0 + s * C::SF_BYTES, a_sf + (a_rt * a_gp4 + a_kc0 + kb) * 512, 512, fb);
+    } else {
+      tma_load_2d(b_dst0 + s * C::B_BYTES, &tm_b, fb, static_cast<int32_t>(b_xoff + kb * BK), static_cast<int32_t>(b_row0));
+#pragma unroll
+      for (int j = 0; j < C::SFB_ATOMS; ++j)
+        bulk_load(sf_dst0 + s * C::SF_BYTES + 512 * (1 + j), b_sf + ((b_rt0 + j) * b_gp4 + b_kc0 + kb) * 512, 512, fb);
+    }
+  };
   // ---- setup ----
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_a);
@@ -313,6 +382,14 @@ __global__ void __launch_bounds__(kThreads, 3)
     *issued_cnt = 0;
     *consumed_cnt = 0;
     fence_mbar_init();
+    // p.early: the first stages need no free slot, so they are issued here, before the TMEM
+    // allocation and the block barrier (launch_gemm decides when)
+    if (p.early)
+      for (int j = 0; j < pre; ++j) {
+        mbar_arrive_expect_tx(bar_full + 8 * j, C::TX_BYTES);
+        load_wt(j, kb_begin + j, bar_full + 8 * j);
+        load_act(j, kb_begin + j, bar_full + 8 * j);
+      }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -332,49 +409,10 @@ __global__ void __launch_bounds__(kThreads, 3)
 
   // ---- roles ----
   if (warp == 0 && lane == 0) {
-    const uint32_t a_dst0 = sbase, b_dst0 = sbase + C::OFF_B, sf_dst0 = sbase + C::OFF_SF;
-    // operand loads of k-block i into stage s; the weight operand is A in swap-AB, B otherwise
-    auto load_act = [&](int s, int kb, uint32_t fb) {
-      if (SWAP && ACT == kActPackedSf) {
-        // E4M3 tile as usual; the stage's packed scale words (one per token, rows b_row0..) into
-        // the staging slot. Only rows < Mp exist in each word column of the packed array.
-        tma_load_2d(b_dst0 + s * C::B_BYTES, &tm_b, fb, static_cast<int32_t>(b_xoff + kb * BK), static_cast<int32_t>(b_row0));
-        const uint32_t ab = bar_act + (fb - bar_full);
-        const int64_t rows = p.act_mp4 - b_row0 < BN ? p.act_mp4 - b_row0 : BN;
-        mbar_arrive_expect_tx(ab, static_cast<uint32_t>(rows * 4));
-        bulk_load(sbase + C::OFF_BF + s * C::BF_BYTES, b_sf + ((b_kc0 + kb) * p.act_mp4 + b_row0) * 4,
-                  static_cast<uint32_t>(rows * 4), ab);
-      } else if (SWAP && CVT) {  // bf16 activations (element coordinates) into the staging slot
-        const uint32_t ab = bar_act + (fb - bar_full);
-        mbar_arrive_expect_tx(ab, C::BF_BYTES);
-        tma_load_2d(sbase + C::OFF_BF + s * C::BF_BYTES, &tm_b, ab, static_cast<int32_t>(b_xoff + kb * BK),
-                    static_cast<int32_t>(b_row0));
-      } else if (SWAP) {
-        tma_load_2d(b_dst0 + s * C::B_BYTES, &tm_b, fb, static_cast<int32_t>(b_xoff + kb * BK), static_cast<int32_t>(b_row0));
-#pragma unroll
-        for (int j = 0; j < C::SFB_ATOMS; ++j)
-          bulk_load(sf_dst0 + s * C::SF_BYTES + 512 * (1 + j), b_sf + ((b_rt0 + j) * b_gp4 + b_kc0 + kb) * 512, 512, fb);
-      } else {
-        tma_load_2d(a_dst0 + s * C::A_BYTES, &tm_a, fb, static_cast<int32_t>(a_xoff + kb * BK), static_cast<int32_t>(a_row0));
-        bulk_load(sf_dst0 + s * C::SF_BYTES, a_sf + (a_rt * a_gp4 + a_kc0 + kb) * 512, 512, fb);
-      }
-    };
-    auto load_wt = [&](int s, int kb, uint32_t fb) {
-      if (SWAP) {
-        tma_load_2d(a_dst0 + s * C::A_BYTES, &tm_a, fb, static_cast<int32_t>(a_xoff + kb * BK), static_cast<int32_t>(a_row0));
-        bulk_load(sf_dst0 + s * C::SF_BYTES, a_sf + (a_rt * a_gp4 + a_kc0 + kb) * 512, 512, fb);
-      } else {
-        tma_load_2d(b_dst0 + s * C::B_BYTES, &tm_b, fb, static_cast<int32_t>(b_xoff + kb * BK), static_cast<int32_t>(b_row0));
-#pragma unroll
-        for (int j = 0; j < C::SFB_ATOMS; ++j)
-          bulk_load(sf_dst0 + s * C::SF_BYTES + 512 * (1 + j), b_sf + ((b_rt0 + j) * b_gp4 + b_kc0 + kb) * 512, 512, fb);
-      }
-    };
-    int i = 0;
+    int i = p.early ? pre : 0;
     if (p.pdl) {
-      // the first STAGES stages are free: fetch their weights while the producer of the
-      // activations may still be running, then wait for it and fetch the activations
-      const int pre = nk < STAGES ? nk : STAGES;
+      // the first stages are free: fetch their weights while the producer of the activations
+      // may still be running (it never writes them), then wait for it and fetch the activations
       for (int j = 0; j < pre; ++j) {
         mbar_arrive_expect_tx(bar_full + 8 * j, C::TX_BYTES);
         load_wt(j, kb_begin + j, bar_full + 8 * j);
@@ -545,25 +583,21 @@ __global__ void __launch_bounds__(kThreads, 3)
         report_timeout(p.status);
       }
       if (!__any_sync(0xffffffffu, *abort_flag)) {
+        // warp q finishes feature group q of this rank's columns, four tokens per pass; lane l
+        // reads feature 32q + l of every slot as 16-byte rows (conflict-free)
         const float* red = reinterpret_cast<const float*>(smem + C::OFF_RECV);
-        const int items = per_rank * 4;
-        for (int w = static_cast<int>(threadIdx.x) - 64; w < items; w += 128) {
-          const int j = w & (per_rank - 1);
-          const int gq = w >> p.per_rank_shift;
-          const int64_t t = b_row0 + static_cast<int>(rank) * per_rank + j;
-          const int64_t col = static_cast<int64_t>(g) * p.n_feat + m0 + 32 * gq;
-          if (t >= p.T) {  // padding token: only its zero scale is stored
-            epi_zero_scale(p, t, col);
-            continue;
-          }
-          float v[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = red[(32 * gq + i) * per_rank + j];
+        const int64_t col = static_cast<int64_t>(g) * p.n_feat + m0 + 32 * q;
+#pragma unroll 1
+        for (int j = 0; j < per_rank; j += 4) {
+          float4 v = *reinterpret_cast<const float4*>(red + f * per_rank + j);
           for (int r = 1; r < p.splits; ++r) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] += red[((r * 128) + 32 * gq + i) * per_rank + j];
+            const float4 u = *reinterpret_cast<const float4*>(red + (r * 128 + f) * per_rank + j);
+            v.x += u.x;
+            v.y += u.y;
+            v.z += u.z;
+            v.w += u.w;
           }
-          epi_token_group(p, v, t, col);
+          epi_group_tokens4(p, v, b_row0 + static_cast<int>(rank) * per_rank + j, col, lane);
         }
       }
     }
@@ -1239,6 +1273,12 @@ cudaError_t launch_gemm(const GemmLaunch& l, cudaStream_t stream) {
   ka.z_mp4 = ceil_div(l.T, 4) * 4;
   ka.status = l.status;
   ka.pdl = l.pdl ? 1 : 0;
+  // The first stages go out during setup, before the TMEM allocation and the block barrier,
+  // except in the decode pair (T <= 16, wo_a followed by its dependent wo_b): standalone calls
+  // and larger pairs gained (T = 1: wo_a 12.8 -> 11.9 us, wo_b 15.2 -> 14.2 us; T = 64 pair
+  // 30.3 -> 30.0 us), while there the earlier wo_a loads made the pair slower (23.6 -> 24.7 us).
+  // A programmatic dependent fetches only weights before its wait, in the producer role.
+  ka.early = (!l.pdl && !(l.T <= 16 && l.has_dependent)) ? 1 : 0;
   ka.act_mp4 = ceil_div(l.T, 4) * 4;
   if (l.n_feat % BM != 0 || l.k_len % BK != 0) return cudaErrorInvalidValue;
   // swap-AB (weights on the MMA's M side) while the token count is small: one token tile of
