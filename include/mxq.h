@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define MXQ_ABI_VERSION 1
+#define MXQ_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define MXQ_API __attribute__((visibility("default")))
@@ -142,6 +142,24 @@ MXQ_API mxq_status rmsnorm_dual_out(const void* x_bf16, const void* gamma_bf16, 
                                     void* stream);
 
 /*
+ * Split workspace of the large-T GEMMs (T > 384). With more than 384 tokens the GEMMs run as
+ * 256 x 256 tiles on pairs of SMs; when the tile count is not a multiple of the pairs, the last
+ * wave would leave pairs idle. Given a workspace, the k-block iterations of all tiles are instead
+ * divided evenly over the pairs, and a pair that starts a tile adds the fp32 partial sums of the
+ * pairs that hold its later k-blocks (in k order: the result does not depend on timing, but may
+ * differ from the no-workspace result in the last bit of a rounding).
+ *
+ * mxq_workspace_bytes() is the size for the current device (two 128 KB fp32 partial slots and
+ * 64 bytes of flags per SM pair, the flags last). The caller owns the buffer (16-byte aligned).
+ * It must be zero-filled before its first use; every call that completes leaves its flags zero
+ * again, so it needs no clearing between calls (after a call that reported MXQ_ERR_TIMEOUT, zero
+ * it again). Calls that overlap in time
+ * (different streams) need separate workspaces; calls ordered on one stream may share one,
+ * including both GEMMs of o_proj_mxfp8. NULL workspace: whole tiles per pair, no partials.
+ */
+MXQ_API int64_t mxq_workspace_bytes(void);
+
+/*
  * wo_a_einsum_mxfp8 -- the grouped wo_a einsum of DeepSeek-V4.1's _o_proj ([MegaAttn]
  * Validation: 8 groups, 4096 in, 1024 out), read as tgk,gnk->tgn:
  *   z[t, g*Na + n] = sum_k deq(o)[t, g*Ka + k] * deq(wa)[g*Na + n, k]   (fp32 accumulation)
@@ -155,12 +173,15 @@ MXQ_API mxq_status rmsnorm_dual_out(const void* x_bf16, const void* gamma_bf16, 
  *   z_sf_packed_i32 : optional second scale layout for z (MXQ_SF_PACKED_I32_MN), or NULL.
  *   z_bf16          : optional bf16 z out ([T, G*Na], row stride G*Na) -- the pre-fusion
  *                     "bf16 z" output, used for validation and the unfused arm; or NULL.
+ *   workspace, workspace_bytes : optional split workspace (mxq_workspace_bytes()), or NULL, 0;
+ *                     a smaller non-NULL workspace returns MXQ_ERR_INVALID_ARG.
  *   status          : optional device status word (mxq_status_bytes()), or NULL.
  * At least one of z_q / z_bf16. Requires Ka % 128 == 0, Na % 128 == 0, G >= 1, T >= 1.
  */
 MXQ_API mxq_status wo_a_einsum_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, int64_t T,
                                      int32_t G, int32_t Na, int32_t Ka, void* z_q, void* z_sf_128x4,
-                                     void* z_sf_packed_i32, void* z_bf16, void* status, void* stream);
+                                     void* z_sf_packed_i32, void* z_bf16, void* workspace,
+                                     int64_t workspace_bytes, void* status, void* stream);
 
 /*
  * gemm_mxfp8_bf16 -- the wo_b MXFP8 GEMM ([MegaAttn] Validation: "wo_b 8192 -> 5120"; it
@@ -171,10 +192,12 @@ MXQ_API mxq_status wo_a_einsum_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor
  *       DeepGEMM-layout consumer), moved into the tensor cores' layout inside the kernel with a
  *       bit-identical result. Packed scales with M > 16 return MXQ_ERR_UNSUPPORTED_SHAPE.
  *   out_bf16 : [M, N] bf16, row stride ldo elements.
+ *   workspace, workspace_bytes : optional split workspace, as in wo_a_einsum_mxfp8.
  * Requires K % 128 == 0, N % 128 == 0, M >= 1.
  */
 MXQ_API mxq_status gemm_mxfp8_bf16(const mxq_mx_tensor* a, const mxq_mx_tensor* b, int64_t M, int64_t N,
-                                   int64_t K, void* out_bf16, int64_t ldo, void* status, void* stream);
+                                   int64_t K, void* out_bf16, int64_t ldo, void* workspace,
+                                   int64_t workspace_bytes, void* status, void* stream);
 
 /*
  * o_proj_mxfp8 -- the fused _o_proj pair ([MegaAttn] Overview): wo_a_einsum_mxfp8 writes z as
@@ -182,12 +205,12 @@ MXQ_API mxq_status gemm_mxfp8_bf16(const mxq_mx_tensor* a, const mxq_mx_tensor* 
  *   out = wo_b( MXFP8( RNE_bf16( einsum(o, wa) ) ) )
  * Two kernel launches, no standalone quantize launch. Arguments as in the two calls above;
  * z_q / z_sf_128x4 are required (the hand-off buffers), z_sf_packed_i32 and z_bf16 optional.
- * out_bf16 : [T, Nb], row stride Nb. Requires Nb % 128 == 0.
+ * out_bf16 : [T, Nb], row stride Nb. Requires Nb % 128 == 0. One workspace serves both GEMMs.
  */
 MXQ_API mxq_status o_proj_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, const mxq_mx_tensor* wb,
                                 int64_t T, int32_t G, int32_t Na, int32_t Ka, int32_t Nb, void* z_q,
                                 void* z_sf_128x4, void* z_sf_packed_i32, void* z_bf16, void* out_bf16,
-                                void* status, void* stream);
+                                void* workspace, int64_t workspace_bytes, void* status, void* stream);
 
 /*
  * mxq_selftest_wait_timeout -- exercises the failure path every kernel shares: one thread waits

@@ -23,4 +23,6 @@ from ._lib import (  # noqa: F401
     sf_bytes,
     status_bytes,
     wo_a_einsum_mxfp8,
+    workspace_bytes,
+    workspace_for,
 )

@@ -56,9 +56,10 @@ SIGNATURES = {
     "mxq_selftest_wait_timeout": ([I64, P, P], ctypes.c_int),
     "mxfp8_quantize": ([P, I64, I64, I64, P, I64, P, P, P, P], ctypes.c_int),
     "rmsnorm_dual_out": ([P, P, ctypes.c_float, I64, I64, I64, P, P, P, P, P, P], ctypes.c_int),
-    "wo_a_einsum_mxfp8": ([_MXP, _MXP, I64, I32, I32, I32, P, P, P, P, P, P], ctypes.c_int),
-    "gemm_mxfp8_bf16": ([_MXP, _MXP, I64, I64, I64, P, I64, P, P], ctypes.c_int),
-    "o_proj_mxfp8": ([_MXP, _MXP, _MXP, I64, I32, I32, I32, I32, P, P, P, P, P, P, P], ctypes.c_int),
+    "mxq_workspace_bytes": ([], I64),
+    "wo_a_einsum_mxfp8": ([_MXP, _MXP, I64, I32, I32, I32, P, P, P, P, P, I64, P, P], ctypes.c_int),
+    "gemm_mxfp8_bf16": ([_MXP, _MXP, I64, I64, I64, P, I64, P, I64, P, P], ctypes.c_int),
+    "o_proj_mxfp8": ([_MXP, _MXP, _MXP, I64, I32, I32, I32, I32, P, P, P, P, P, P, I64, P, P], ctypes.c_int),
     "o_proj_mxfp8_noalloc": ([_MXP, _MXP, _MXP, I64, I32, I32, I32, I32, P, P, P], ctypes.c_int),
     "o_proj_mxfp8_from_bf16": ([P, I64, _MXP, _MXP, I64, I32, I32, I32, I32, P, P, P, P, P, P, P], ctypes.c_int),
 }
@@ -107,6 +108,40 @@ def _check(status: int, where: str):
 
 def abi_version() -> int:
     return int(load().mxq_abi_version())
+
+
+def workspace_bytes() -> int:
+    """Bytes of the split workspace of the large-T GEMMs on the current device."""
+    return int(load().mxq_workspace_bytes())
+
+
+_workspaces = {}
+
+
+def workspace_for(stream=None) -> Optional[torch.Tensor]:
+    """The zero-filled split workspace this module keeps for one CUDA stream, created on its
+    first use. Calls ordered on one stream may share it (the library leaves its flags zero);
+    concurrent streams each get their own. Under stream capture a workspace is not created (the
+    capture would own its memory): there it is None unless a call on the same stream made it
+    before the capture began."""
+    s = torch.cuda.current_stream() if stream is None else stream
+    key = (s.device.index if hasattr(s, "device") else torch.cuda.current_device(), _stream(s).value)
+    ws = _workspaces.get(key)
+    if ws is None:
+        if torch.cuda.is_current_stream_capturing():
+            return None
+        ws = torch.zeros(workspace_bytes(), dtype=torch.uint8, device=s.device if hasattr(s, "device") else "cuda")
+        _workspaces[key] = ws
+    return ws
+
+
+def _ws(workspace, stream):
+    """(pointer, bytes) for a workspace argument: None = this stream's own, False = none."""
+    if workspace is None:
+        workspace = workspace_for(stream)
+    if workspace is None or workspace is False:
+        return None, 0
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
 
 
 def sf_bytes(layout: int, M: int, K: int) -> int:
@@ -176,27 +211,31 @@ def rmsnorm_dual_out(x: torch.Tensor, gamma: torch.Tensor, eps: float, y: torch.
 
 
 def wo_a_einsum_mxfp8(o: MXFP8, wa: MXFP8, T: int, G: int, Na: int, Ka: int, z_q=None, z_sf_128x4=None,
-                      z_sf_packed=None, z_bf16=None, status=None, stream=None) -> None:
+                      z_sf_packed=None, z_bf16=None, status=None, stream=None, workspace=None) -> None:
+    """workspace: None = the stream's own split workspace, False = none, or a tensor."""
     oc, wc = o.c(), wa.c()
+    wp, wn = _ws(workspace, stream)
     _check(load().wo_a_einsum_mxfp8(ctypes.byref(oc), ctypes.byref(wc), T, G, Na, Ka, _ptr(z_q), _ptr(z_sf_128x4),
-                                    _ptr(z_sf_packed), _ptr(z_bf16), _ptr(status), _stream(stream)),
+                                    _ptr(z_sf_packed), _ptr(z_bf16), wp, wn, _ptr(status), _stream(stream)),
            "wo_a_einsum_mxfp8")
 
 
-def gemm_mxfp8_bf16(a: MXFP8, b: MXFP8, out: torch.Tensor, status=None, stream=None) -> None:
+def gemm_mxfp8_bf16(a: MXFP8, b: MXFP8, out: torch.Tensor, status=None, stream=None, workspace=None) -> None:
     M, K = a.data.shape
     N = b.data.shape[0]
     assert out.dtype == torch.bfloat16 and out.stride(1) == 1
     ac, bc = a.c(), b.c()
-    _check(load().gemm_mxfp8_bf16(ctypes.byref(ac), ctypes.byref(bc), M, N, K, _ptr(out), out.stride(0),
+    wp, wn = _ws(workspace, stream)
+    _check(load().gemm_mxfp8_bf16(ctypes.byref(ac), ctypes.byref(bc), M, N, K, _ptr(out), out.stride(0), wp, wn,
                                   _ptr(status), _stream(stream)), "gemm_mxfp8_bf16")
 
 
 def o_proj_mxfp8(o: MXFP8, wa: MXFP8, wb: MXFP8, T: int, G: int, Na: int, Ka: int, Nb: int, z_q, z_sf_128x4,
-                 out: torch.Tensor, z_sf_packed=None, z_bf16=None, status=None, stream=None) -> None:
+                 out: torch.Tensor, z_sf_packed=None, z_bf16=None, status=None, stream=None, workspace=None) -> None:
     oc, ac, bc = o.c(), wa.c(), wb.c()
+    wp, wn = _ws(workspace, stream)
     _check(load().o_proj_mxfp8(ctypes.byref(oc), ctypes.byref(ac), ctypes.byref(bc), T, G, Na, Ka, Nb, _ptr(z_q),
-                               _ptr(z_sf_128x4), _ptr(z_sf_packed), _ptr(z_bf16), _ptr(out), _ptr(status),
+                               _ptr(z_sf_128x4), _ptr(z_sf_packed), _ptr(z_bf16), _ptr(out), wp, wn, _ptr(status),
                                _stream(stream)), "o_proj_mxfp8")
 
 

@@ -132,9 +132,16 @@ mxq_status rmsnorm_dual_out(const void* x_bf16, const void* gamma_bf16, float ep
 
 namespace {
 
+// optional split workspace: NULL, or 16-byte aligned and at least mxq_workspace_bytes()
+mxq_status check_workspace(const void* ws, int64_t bytes) {
+  if (ws == nullptr) return MXQ_OK;
+  if (!al16(ws)) return MXQ_ERR_MISALIGNED;
+  return bytes >= mxq::split_workspace_bytes() ? MXQ_OK : MXQ_ERR_INVALID_ARG;
+}
+
 mxq_status wo_a_impl(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, int64_t T, int32_t G, int32_t Na, int32_t Ka,
-                     void* z_q, void* z_sf_128x4, void* z_sf_packed_i32, void* z_bf16, void* status, void* stream,
-                     bool has_dependent) {
+                     void* z_q, void* z_sf_128x4, void* z_sf_packed_i32, void* z_bf16, void* ws, int64_t ws_bytes,
+                     void* status, void* stream, bool has_dependent) {
   if (T <= 0 || G <= 0 || Na <= 0 || Ka <= 0) return MXQ_ERR_INVALID_ARG;
   if ((z_q == nullptr) != (z_sf_128x4 == nullptr)) return MXQ_ERR_INVALID_ARG;
   if (z_q == nullptr && z_bf16 == nullptr) return MXQ_ERR_INVALID_ARG;
@@ -148,7 +155,10 @@ mxq_status wo_a_impl(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, int64_t T,
   if ((st = check_operand(wa, static_cast<int64_t>(G) * Na, Ka)) != MXQ_OK) return st;
   if (!al16(z_q) || !al16(z_sf_128x4) || !al16(z_sf_packed_i32) || !al16(z_bf16) || !al16(status))
     return MXQ_ERR_MISALIGNED;
+  if ((st = check_workspace(ws, ws_bytes)) != MXQ_OK) return st;
   mxq::GemmLaunch l = {};
+  l.workspace = ws;
+  l.workspace_bytes = ws_bytes;
   l.act = o->data;
   l.act_sf = o->sf;
   l.act_cols = o->cols;
@@ -175,10 +185,13 @@ mxq_status wo_a_impl(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, int64_t T,
 
 extern "C" {
 
+int64_t mxq_workspace_bytes(void) { return mxq::split_workspace_bytes(); }
+
 mxq_status wo_a_einsum_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, int64_t T, int32_t G, int32_t Na,
                              int32_t Ka, void* z_q, void* z_sf_128x4, void* z_sf_packed_i32, void* z_bf16,
-                             void* status, void* stream) {
-  return wo_a_impl(o, wa, T, G, Na, Ka, z_q, z_sf_128x4, z_sf_packed_i32, z_bf16, status, stream, false);
+                             void* workspace, int64_t workspace_bytes, void* status, void* stream) {
+  return wo_a_impl(o, wa, T, G, Na, Ka, z_q, z_sf_128x4, z_sf_packed_i32, z_bf16, workspace, workspace_bytes, status,
+                   stream, false);
 }
 
 }  // extern "C"
@@ -189,7 +202,7 @@ namespace {
 // dependent of the previous kernel on the stream; only o_proj_mxfp8 sets it, because only
 // there is that kernel known (its own wo_a, which never writes the weights wo_b prefetches).
 mxq_status gemm_impl(const mxq_mx_tensor* a, const mxq_mx_tensor* b, int64_t M, int64_t N, int64_t K, void* out_bf16,
-                     int64_t ldo, void* status, void* stream, bool pdl) {
+                     int64_t ldo, void* ws, int64_t ws_bytes, void* status, void* stream, bool pdl) {
   if (M <= 0 || N <= 0 || K <= 0 || out_bf16 == nullptr) return MXQ_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % 128 != 0 || ldo < N) return MXQ_ERR_UNSUPPORTED_SHAPE;
   if (N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return MXQ_ERR_UNSUPPORTED_SHAPE;
@@ -205,7 +218,10 @@ mxq_status gemm_impl(const mxq_mx_tensor* a, const mxq_mx_tensor* b, int64_t M, 
   }
   if ((st = check_operand(b, N, K)) != MXQ_OK) return st;
   if (!al16(out_bf16) || !al16(status) || (ldo * 2) % 16 != 0) return MXQ_ERR_MISALIGNED;
+  if ((st = check_workspace(ws, ws_bytes)) != MXQ_OK) return st;
   mxq::GemmLaunch l = {};
+  l.workspace = ws;
+  l.workspace_bytes = ws_bytes;
   l.act = a->data;
   l.act_sf = a->sf;
   l.act_cols = a->cols;
@@ -231,13 +247,15 @@ mxq_status gemm_impl(const mxq_mx_tensor* a, const mxq_mx_tensor* b, int64_t M, 
 extern "C" {
 
 mxq_status gemm_mxfp8_bf16(const mxq_mx_tensor* a, const mxq_mx_tensor* b, int64_t M, int64_t N, int64_t K,
-                           void* out_bf16, int64_t ldo, void* status, void* stream) {
-  return gemm_impl(a, b, M, N, K, out_bf16, ldo, status, stream, false);
+                           void* out_bf16, int64_t ldo, void* workspace, int64_t workspace_bytes, void* status,
+                           void* stream) {
+  return gemm_impl(a, b, M, N, K, out_bf16, ldo, workspace, workspace_bytes, status, stream, false);
 }
 
 mxq_status o_proj_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, const mxq_mx_tensor* wb, int64_t T,
                         int32_t G, int32_t Na, int32_t Ka, int32_t Nb, void* z_q, void* z_sf_128x4,
-                        void* z_sf_packed_i32, void* z_bf16, void* out_bf16, void* status, void* stream) {
+                        void* z_sf_packed_i32, void* z_bf16, void* out_bf16, void* workspace, int64_t workspace_bytes,
+                        void* status, void* stream) {
   if (z_q == nullptr || z_sf_128x4 == nullptr || out_bf16 == nullptr) return MXQ_ERR_INVALID_ARG;
   if (Nb <= 0 || G <= 0 || Na <= 0) return MXQ_ERR_INVALID_ARG;
   if (Nb % 128 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
@@ -245,10 +263,12 @@ mxq_status o_proj_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, const m
   mxq_status st = check_operand(wb, Nb, Kb);
   if (st != MXQ_OK) return st;
   if (!al16(out_bf16)) return MXQ_ERR_MISALIGNED;
-  st = wo_a_impl(o, wa, T, G, Na, Ka, z_q, z_sf_128x4, z_sf_packed_i32, z_bf16, status, stream, true);
+  if ((st = check_workspace(workspace, workspace_bytes)) != MXQ_OK) return st;
+  st = wo_a_impl(o, wa, T, G, Na, Ka, z_q, z_sf_128x4, z_sf_packed_i32, z_bf16, workspace, workspace_bytes, status,
+                 stream, true);
   if (st != MXQ_OK) return st;
   const mxq_mx_tensor z = {z_q, z_sf_128x4, MXQ_SF_TILED_128X4, T, Kb, Kb};
-  return gemm_impl(&z, wb, T, Nb, Kb, out_bf16, Nb, status, stream, true);
+  return gemm_impl(&z, wb, T, Nb, Kb, out_bf16, Nb, workspace, workspace_bytes, status, stream, true);
 }
 
 mxq_status o_proj_mxfp8_from_bf16(const void* o_bf16, int64_t ld_o, const mxq_mx_tensor* wa, const mxq_mx_tensor* wb,
@@ -289,7 +309,7 @@ mxq_status o_proj_mxfp8_from_bf16(const void* o_bf16, int64_t ld_o, const mxq_mx
   st = from_cuda(mxq::launch_gemm(l, static_cast<cudaStream_t>(stream)));
   if (st != MXQ_OK) return st;
   const mxq_mx_tensor z = {z_q, z_sf_128x4, MXQ_SF_TILED_128X4, T, Kb, Kb};
-  return gemm_impl(&z, wb, T, Nb, Kb, out_bf16, Nb, status, stream, true);
+  return gemm_impl(&z, wb, T, Nb, Kb, out_bf16, Nb, nullptr, 0, status, stream, true);
 }
 
 mxq_status mxq_selftest_wait_timeout(int64_t limit_us, void* status, void* stream) {

@@ -39,6 +39,9 @@ constexpr int BM = 128;            // MMA M: rows of the A operand = TMEM lanes
 constexpr int BK = 128;            // K bytes per stage = one 128-byte swizzle row
 constexpr int kStatusTimeout = 6;  // MXQ_ERR_TIMEOUT
 constexpr int kSwapMaxTokens = 384; // above this the CTA-pair kernel is faster (measured, T = 512)
+// Fixed cost of the stream-K tail (partial sums through L2, flags, the finishing pass), in
+// k-blocks of tile time: the split is taken only when whole tiles would waste more than this.
+constexpr int kSkCostKb = 16;
 
 struct KArgs {
   int64_t T;
@@ -64,6 +67,11 @@ struct KArgs {
   int64_t z_mp4;
   int32_t* status;
   int64_t act_mp4;  // packed activation scales: rows per word column (ceil(T / 4) * 4)
+  // CTA-pair kernel, stream-K mode (null: round robin over whole tiles). Partial sums of the
+  // segments that do not start a tile: one 128 KB slot per CTA, [pair][rank][64 x 16-byte
+  // columns][128 rows]; ready flags [pair][rank][8 epilogue warps], zero between launches.
+  float4* sk_part;
+  int32_t* sk_flag;
 };
 
 __device__ __forceinline__ void report_timeout(int32_t* status) {
@@ -811,8 +819,9 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   // Work items, taken round robin by the pairs: the 256 x 256 tiles of the full waves, then, when
   // the last wave would leave more than half the pairs idle, its tiles as two 256 x 128 halves
   // each, which that wave spreads over twice as many pairs.
+  const bool sk = p.sk_part != nullptr;
   const int tail = total % tile_step;
-  const bool split_tail = tail > 0 && 2 * tail <= tile_step;
+  const bool split_tail = !sk && tail > 0 && 2 * tail <= tile_step;
   const int n_items = split_tail ? total + tail : total;
   // item -> (group, first token of the 256-token pair tile, first feature, features)
   auto item = [&](int i, int& g, int64_t& m0, int64_t& n0, int& nf) {
@@ -828,6 +837,50 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     const int r = t - g * per_group;
     m0 = static_cast<int64_t>(r / n_tiles) * (2 * BM);
     n0 = static_cast<int64_t>(r % n_tiles) * BN + hf * (BN / 2);
+  };
+  // Stream-K mode: all but the last full wave of whole tiles are taken round robin as above (pairs
+  // that run at the same time work on neighbouring tiles, which share operands in L2); the
+  // k-block iterations of the remaining tiles are cut into one contiguous range per pair,
+  // [I * pair / P, I * (pair + 1) / P). Such a range starts inside a tile and may end inside one:
+  // its segments are (tile, k-blocks [kb_lo, kb_hi)). The pair whose segment starts a tile
+  // (kb_lo == 0) finishes it, adding the partial sums of the later pairs that hold the rest of its
+  // k-blocks, in k order (deterministic); those write theirs to the workspace first thing.
+  const int pair = static_cast<int>(blockIdx.x >> 1), n_pairs = tile_step;
+  // the split tail is the last wave of whole tiles plus the remainder, so that every pair's range
+  // covers at least one tile's worth of k-blocks and few pairs share a tile
+  const int full_waves = sk && total / n_pairs > 0 ? total / n_pairs - 1 : 0;
+  const int tail0 = full_waves * n_pairs;  // first tile of the split tail
+  const int64_t iters = static_cast<int64_t>(total - tail0) * nk;
+  auto range_lo = [&](int q_) { return iters * q_ / n_pairs; };
+  const int64_t sk_lo = range_lo(pair), sk_hi = range_lo(pair + 1);
+  // segment w of this pair (work item w in round-robin mode); false past the last one
+  auto seg = [&](int w, int& t, int& g, int64_t& m0, int64_t& n0, int& nf, int& kb_lo, int& kb_hi) -> bool {
+    if (!sk) {
+      t = first_tile + w * tile_step;
+      if (t >= n_items) return false;
+      item(t, g, m0, n0, nf);
+      kb_lo = 0;
+      kb_hi = nk;
+      return true;
+    }
+    if (w < full_waves) {
+      t = pair + w * n_pairs;
+      kb_lo = 0;
+      kb_hi = nk;
+    } else {
+      const int64_t tt = sk_lo / nk + (w - full_waves);  // tail tile, counted from tail0
+      const int64_t start = w == full_waves ? sk_lo : tt * nk;
+      if (start >= sk_hi) return false;
+      kb_lo = static_cast<int>(start - tt * nk);
+      kb_hi = static_cast<int>(sk_hi - tt * nk < nk ? sk_hi - tt * nk : nk);
+      t = tail0 + static_cast<int>(tt);
+    }
+    g = t / per_group;
+    const int r = t - g * per_group;
+    m0 = static_cast<int64_t>(r / n_tiles) * (2 * BM);
+    n0 = static_cast<int64_t>(r % n_tiles) * BN;
+    nf = BN;
+    return true;
   };
 
   if (warp == 0 && lane == 0) {
@@ -864,10 +917,10 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     const uint32_t full0 = mapa_shared(bar_full, 0);  // the even CTA's stage barriers
     int it = 0;
     bool first = true;
-    for (int i = first_tile; i < n_items && !*abort_flag; i += tile_step) {
-      int g, nf;
+    for (int w = 0; !*abort_flag; ++w) {
+      int t, g, nf, kb_lo, kb_hi;
       int64_t m0, n0;
-      item(i, g, m0, n0, nf);
+      if (!seg(w, t, g, m0, n0, nf, kb_lo, kb_hi)) break;
       const uint32_t tx = C::tx_bytes(nf);
       const int64_t a_row = m0 + BM * rank;  // this CTA's token rows
       const int64_t a_x = static_cast<int64_t>(g) * p.act_k_per_group;
@@ -886,20 +939,20 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         tma_load_2d_pair(sf + 512, &tm_sfb, fb, 0, static_cast<int32_t>(b_atom + kb));
         if (nf == BN) tma_load_2d_pair(sf + 1024, &tm_sfb, fb, 0, static_cast<int32_t>(b_atom + p.wt_gp4 + kb));
       };
-      int kb = 0;
+      int kb = kb_lo;
       if (first && p.pdl) {
-        const int pre = nk < STAGES ? nk : STAGES;
+        const int pre = kb_hi - kb_lo < STAGES ? kb_hi - kb_lo : STAGES;
         for (int j = 0; j < pre; ++j) {
           if (leader) mbar_arrive_expect_tx(bar_full + 8 * j, tx);
-          load_wt(j, j, full0 + 8 * j);
+          load_wt(j, kb_lo + j, full0 + 8 * j);
         }
         pdl_wait_primary();
-        for (int j = 0; j < pre; ++j) load_act(j, j, full0 + 8 * j);
-        kb = pre;
+        for (int j = 0; j < pre; ++j) load_act(j, kb_lo + j, full0 + 8 * j);
+        kb = kb_lo + pre;
         it = pre;
       }
       first = false;
-      for (; kb < nk; ++kb, ++it) {
+      for (; kb < kb_hi; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
         if (!mbar_wait_bounded(bar_empty + 8 * s, ph ^ 1)) {
@@ -920,10 +973,10 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       // soon as the stage's operands have landed: the copies are issued by another thread, so
       // this thread's MMA stream never waits behind a copy of its own.
       int it = 0, ti = 0;
-      for (int i = first_tile; i < n_items && !*abort_flag; i += tile_step, ++ti) {
-        int g, nf;
+      for (int w = 0; !*abort_flag; ++w, ++ti) {
+        int t, g, nf, kb_lo, kb_hi;
         int64_t m0, n0;
-        item(i, g, m0, n0, nf);
+        if (!seg(w, t, g, m0, n0, nf, kb_lo, kb_hi)) break;
         if (!mbar_wait_bounded(bar_acce, (ti & 1) ^ 1)) {  // both halves drained by the epilogues
           *abort_flag = 1;
           report_timeout(p.status);
@@ -931,7 +984,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         }
         tc_fence_after();
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
           const int s = it % STAGES;
           if (!mbar_wait_bounded(bar_sf + 8 * s, (it / STAGES) & 1)) {
             *abort_flag = 1;
@@ -947,7 +1000,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
             tc_mma_mxf8_pair(tmem, ad + 2 * k, bd + 2 * k, idesc_mxf8(2 * BM, static_cast<uint32_t>(nf), k, k), sfa_t,
-                             sfb_t, (kb | k) != 0 ? 1u : 0u);
+                             sfb_t, (kb != kb_lo || k != 0) ? 1u : 0u);
           tc_commit_pair(bar_empty + 8 * s, 0x3);
         }
         tc_commit_pair(bar_accf, 0x3);
@@ -960,9 +1013,12 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     // ---------------- scale copies (even CTA) ----------------
     if (leader && lane == 0) {
       int it = 0;
-      for (int i = first_tile; i < n_items && !*abort_flag; i += tile_step) {
-        const bool full_tile = !(split_tail && i >= total - tail);
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+      for (int w = 0; !*abort_flag; ++w) {
+        int t, g, nf, kb_lo, kb_hi;
+        int64_t m0, n0;
+        if (!seg(w, t, g, m0, n0, nf, kb_lo, kb_hi)) break;
+        const bool full_tile = nf == BN;
+        for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
           const int s = it % STAGES;
           if (!mbar_wait_bounded(bar_full + 8 * s, (it / STAGES) & 1)) {
             *abort_flag = 1;
@@ -985,11 +1041,12 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     const int half = (warp - 2) >> 2;  // accumulator columns [128*half, 128*half + 128)
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16) + 128 * half;
     const uint32_t acce0 = mapa_shared(bar_acce, 0);
+    const int ew = warp - 2;  // this warp's share of a partial slot and its ready flag
     int ti = 0;
-    for (int i = first_tile; i < n_items; i += tile_step, ++ti) {
-      int g, nf;
+    for (int w = 0;; ++w, ++ti) {
+      int t, g, nf, kb_lo, kb_hi;
       int64_t m0, n0;
-      item(i, g, m0, n0, nf);
+      if (!seg(w, t, g, m0, n0, nf, kb_lo, kb_hi)) break;
       if (!mbar_wait_bounded(bar_accf, ti & 1)) {
         *abort_flag = 1;
         report_timeout(p.status);
@@ -1005,6 +1062,69 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         continue;
       }
       tc_fence_after();
+      const int64_t row0 = m0 + BM * rank;
+      const int64_t row = row0 + 32 * q + lane;
+      const int64_t col0 = static_cast<int64_t>(g) * p.n_feat + n0 + 128 * half;
+      // Partial slots are [pair][rank][8 warps][32 x 16-byte column groups][32 lanes]: a warp's
+      // 16 KB are contiguous and each of its 16-byte stores or loads covers 512 contiguous bytes.
+      // Rows past the last token hold zeros on both sides and are neither stored nor loaded.
+      const bool live = row < p.T;
+      auto slot_of = [&](int pr) {
+        return p.sk_part + (static_cast<int64_t>(pr * 2 + static_cast<int>(rank)) * 8 + ew) * (32 * 32) + lane;
+      };
+      if (sk && kb_lo == 0 && kb_hi < nk && row0 < p.z_mp128) {
+        // This segment starts a tile of the split tail (always the pair's last segment, so the
+        // accumulator may stay in TMEM): take each later pair's partial as its flag rises, 16
+        // columns' loads in flight per contributor, and add it in k order, chunk by chunk.
+        const int64_t end = (static_cast<int64_t>(t - tail0) + 1) * nk;
+        int p_end = pair + 1;  // the contributors are the pairs pair + 1 .. p_end - 1
+        while (p_end < n_pairs && range_lo(p_end) < end) ++p_end;
+        bool ok = true;
+        for (int p2 = pair + 1; p2 < p_end && ok; ++p2) {
+          if (range_lo(p2 + 1) == range_lo(p2)) continue;  // an empty range holds nothing
+          if (lane == 0) ok = wait_flag_gpu(p.sk_flag + (p2 * 2 + static_cast<int>(rank)) * 8 + ew);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        }
+        if (!ok) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            report_timeout(p.status);
+          }
+          break;
+        }
+        uint32_t word = 0;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t a[32];
+          tmem_ld_x32(t_lane + 32 * c, a);
+          tmem_ld_wait();
+          for (int p2 = pair + 1; p2 < p_end && live; ++p2) {
+            if (range_lo(p2 + 1) == range_lo(p2)) continue;
+            const float4* src = slot_of(p2) + c * 8 * 32;
+            float4 u[8];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) u[v] = __ldcg(src + v * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              a[4 * v] = __float_as_uint(__uint_as_float(a[4 * v]) + u[v].x);
+              a[4 * v + 1] = __float_as_uint(__uint_as_float(a[4 * v + 1]) + u[v].y);
+              a[4 * v + 2] = __float_as_uint(__uint_as_float(a[4 * v + 2]) + u[v].z);
+              a[4 * v + 3] = __float_as_uint(__uint_as_float(a[4 * v + 3]) + u[v].w);
+            }
+          }
+          epi_row_chunk(p, a, row, col0 + 32 * c, word, c);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          for (int p2 = pair + 1; p2 < p_end; ++p2) p.sk_flag[(p2 * 2 + static_cast<int>(rank)) * 8 + ew] = 0;
+          if (leader)
+            mbar_arrive(bar_acce);
+          else
+            mbar_arrive_remote(acce0);
+        }
+        continue;
+      }
       uint32_t acc[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_x32(t_lane + 32 * c, acc[c]);
@@ -1017,10 +1137,25 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         else
           mbar_arrive_remote(acce0);
       }
-      const int64_t row0 = m0 + BM * rank;
       if (row0 >= p.z_mp128) continue;  // this half of a ragged last pair tile holds no token
-      const int64_t row = row0 + 32 * q + lane;
-      const int64_t col0 = static_cast<int64_t>(g) * p.n_feat + n0 + 128 * half;
+      if (sk && kb_lo > 0) {
+        // a later part of a tile's k-blocks: this warp's 32 rows x 128 columns of fp32 partial
+        // sums go to the pair's slot, then its flag rises for the pair that finishes the tile
+        if (live) {
+          float4* dst = slot_of(pair);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              __stcg(dst + (c * 8 + v) * 32,
+                     make_float4(__uint_as_float(acc[c][4 * v]), __uint_as_float(acc[c][4 * v + 1]),
+                                 __uint_as_float(acc[c][4 * v + 2]), __uint_as_float(acc[c][4 * v + 3])));
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(p.sk_flag + (pair * 2 + static_cast<int>(rank)) * 8 + ew, 1);
+        continue;
+      }
       uint32_t word = 0;
 #pragma unroll
       for (int c = 0; c < 4; ++c) epi_row_chunk(p, acc[c], row, col0 + 32 * c, word, c);
@@ -1210,6 +1345,35 @@ cudaError_t launch_normal(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
 
 }  // namespace
 
+constexpr int64_t kSkSlotBytes = 2 * 128 * 256 * 4;  // one pair: two CTAs' 128 x 256 fp32 partials
+constexpr int64_t kSkFlagBytes = 2 * 8 * 4;          // one pair: two CTAs x 8 epilogue warps
+
+// Clusters of the pair kernel that fit on the device at once (1 CTA per SM by its shared memory).
+template <int STAGES>
+int pair_clusters_resident() {
+  static const int n = [] {
+    using C = PairCfg<STAGES>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms()), 1, 1);
+    cfg.blockDim = dim3(kThreadsPair, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_mxf8_pair<STAGES>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return 0;
+    }
+    return clusters;
+  }();
+  return n;
+}
+
 // CTA-pair persistent launch: clusters of two, one CTA per SM, pair tiles of 256 x 256
 template <int STAGES>
 cudaError_t launch_pair(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
@@ -1224,7 +1388,29 @@ cudaError_t launch_pair(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   // With fewer tiles than half the pairs, launch two pairs per tile: the kernel then runs every
   // tile as two 256 x 128 halves (its last-wave split), one per pair.
   const int64_t want = 2 * tiles <= max_pairs ? 2 * tiles : tiles;
-  const int pairs = static_cast<int>(want < max_pairs ? want : max_pairs);
+  int pairs = static_cast<int>(want < max_pairs ? want : max_pairs);
+  // Stream-K when a workspace is given and whole tiles would leave a ragged last wave that costs
+  // more than the split's fixed cost: every pair that can be resident at once then takes an
+  // equal share of the tail's k-block iterations (all of them must be resident together, since a
+  // pair that starts a tile waits for the partials of the pairs after it). Whole tiles take
+  // floor(tiles / P) waves plus half a tile (the last wave split in two halves) or a whole one;
+  // measured: wo_b (64 k-blocks) gains at 1024..4096 tokens, wo_a (32 k-blocks) never does.
+  if (l.workspace != nullptr && tiles % max_pairs != 0) {
+    const int resident = pair_clusters_resident<STAGES>();
+    const int sk_pairs = resident < max_pairs ? resident : max_pairs;
+    const int64_t rem = sk_pairs > 0 ? tiles % sk_pairs : 0;
+    const double rr_tail = rem == 0 ? 0.0 : (2 * rem <= sk_pairs ? 0.5 : 1.0);
+    const double waste_kb = (rr_tail - static_cast<double>(rem) / sk_pairs) * ka.kb_per_cta;
+    // (with fewer tiles than pairs a pair holds less than a tile and many pairs share each one:
+    // the partials cost more than the split saves, measured at T = 512)
+    // Past 8 waves the tail is a small share of the launch: whole tiles then.
+    if (sk_pairs >= 2 && tiles >= sk_pairs && tiles <= 8 * sk_pairs && waste_kb > kSkCostKb) {
+      uint8_t* ws = static_cast<uint8_t*>(l.workspace);
+      ka.sk_part = reinterpret_cast<float4*>(ws);
+      ka.sk_flag = reinterpret_cast<int32_t*>(ws + static_cast<int64_t>(max_pairs) * kSkSlotBytes);
+      pairs = sk_pairs;
+    }
+  }
   CUtensorMap tma_act, tma_wt, tma_wt64, tma_sfa, tma_sfb;
   if (!make_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, BM)) return cudaErrorInvalidValue;
   if (!make_map(&tma_wt, l.wt, static_cast<int64_t>(l.G) * l.n_feat, l.k_len, l.wt_ld, 128)) return cudaErrorInvalidValue;
@@ -1252,6 +1438,8 @@ cudaError_t launch_pair(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, kern, tma_act, tma_wt, tma_wt64, tma_sfa, tma_sfb, ka);
 }
 
+int64_t split_workspace_bytes() { return static_cast<int64_t>(num_sms() / 2) * (kSkSlotBytes + kSkFlagBytes); }
+
 cudaError_t launch_gemm(const GemmLaunch& l, cudaStream_t stream) {
   KArgs ka = {};
   ka.T = l.T;
@@ -1273,6 +1461,7 @@ cudaError_t launch_gemm(const GemmLaunch& l, cudaStream_t stream) {
   ka.z_mp4 = ceil_div(l.T, 4) * 4;
   ka.status = l.status;
   ka.pdl = l.pdl ? 1 : 0;
+  if (l.workspace != nullptr && l.workspace_bytes < split_workspace_bytes()) return cudaErrorInvalidValue;
   // The first stages go out during setup, before the TMEM allocation and the block barrier,
   // except in the decode pair (T <= 16, wo_a followed by its dependent wo_b): standalone calls
   // and larger pairs gained (T = 1: wo_a 12.8 -> 11.9 us, wo_b 15.2 -> 14.2 us; T = 64 pair

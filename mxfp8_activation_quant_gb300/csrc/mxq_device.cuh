@@ -127,6 +127,29 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
   return mbar_wait_limit(bar, parity, kWaitLimitNs);
 }
 
+// Global-memory flags between CTAs of one grid: release store, acquire load, and a bounded wait
+// (about a second) for a nonzero value.
+__device__ __forceinline__ void st_release_gpu(int32_t* p, int32_t v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool wait_flag_gpu(const int32_t* p) {
+  if (ld_acquire_gpu(p) != 0) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i) {
+      __nanosleep(32);
+      if (ld_acquire_gpu(p) != 0) return true;
+    }
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 // ------------------------------------------------------------------------------------------
 // TMA
 // ------------------------------------------------------------------------------------------

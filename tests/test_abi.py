@@ -27,17 +27,19 @@ def test_every_declared_symbol_is_exported(lib):
     from mxfp8_activation_quant_gb300 import _lib
 
     names = declared_functions()
-    assert len(names) == 14, names
+    assert len(names) == 15, names
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(_lib.SIGNATURES)
 
 
 def test_version_and_status_strings(lib):
-    assert lib.mxq_abi_version() == 1
+    assert lib.mxq_abi_version() == 2
     for code, name in [(0, b"MXQ_OK"), (2, b"MXQ_ERR_UNSUPPORTED_SHAPE"), (6, b"MXQ_ERR_TIMEOUT")]:
         assert lib.mxq_status_string(code) == name
     assert lib.mxq_status_bytes() >= 4
+    # two 128 KB partial slots and 64 bytes of flags per SM pair
+    assert lib.mxq_workspace_bytes() > 0 and lib.mxq_workspace_bytes() % (2 * 128 * 1024 + 64) == 0
 
 
 def test_sf_bytes_match_oracle_layout_sizes(lib, oracle):
@@ -85,20 +87,26 @@ def test_gemm_argument_errors(lib):
     o, wa, wb = mx(8, 32768), mx(8192, 4096), mx(5120, 8192)
     B = ctypes.byref
     e = lib.wo_a_einsum_mxfp8
-    assert e(B(o), B(wa), 8, 8, 1024, 4096, FAKE, None, None, None, None, None) == 1    # z_q w/o scales
-    assert e(B(o), B(wa), 8, 8, 1024, 4096, None, None, None, None, None, None) == 1    # no output
-    assert e(B(mx(8, 32768, layout=0)), B(wa), 8, 8, 1024, 4096, FAKE, FAKE, None, None, None, None) == 4
-    assert e(B(o), B(wa), 8, 8, 1000, 4096, FAKE, FAKE, None, None, None, None) == 2    # Na % 128
-    assert e(B(o), B(wa), 9, 8, 1024, 4096, FAKE, FAKE, None, None, None, None) == 2    # rows != T
-    assert e(B(mx(8, 32768, data=FAKE + 1)), B(wa), 8, 8, 1024, 4096, FAKE, FAKE, None, None, None, None) == 3
+    W0 = (None, 0)  # no split workspace
+    assert e(B(o), B(wa), 8, 8, 1024, 4096, FAKE, None, None, None, *W0, None, None) == 1    # z_q w/o scales
+    assert e(B(o), B(wa), 8, 8, 1024, 4096, None, None, None, None, *W0, None, None) == 1    # no output
+    assert e(B(mx(8, 32768, layout=0)), B(wa), 8, 8, 1024, 4096, FAKE, FAKE, None, None, *W0, None, None) == 4
+    assert e(B(o), B(wa), 8, 8, 1000, 4096, FAKE, FAKE, None, None, *W0, None, None) == 2    # Na % 128
+    assert e(B(o), B(wa), 9, 8, 1024, 4096, FAKE, FAKE, None, None, *W0, None, None) == 2    # rows != T
+    assert e(B(mx(8, 32768, data=FAKE + 1)), B(wa), 8, 8, 1024, 4096, FAKE, FAKE, None, None, *W0, None, None) == 3
+    assert e(B(o), B(wa), 8, 8, 1024, 4096, FAKE, FAKE, None, None, FAKE, 16, None, None) == 1  # workspace too small
+    assert e(B(o), B(wa), 8, 8, 1024, 4096, FAKE, FAKE, None, None, FAKE + 8, 1 << 30, None, None) == 3
     g = lib.gemm_mxfp8_bf16
-    assert g(B(mx(8, 8192)), B(wb), 8, 5120, 8192, None, 5120, None, None) == 1
-    assert g(B(mx(8, 8192)), B(mx(5000, 8192)), 8, 5000, 8192, FAKE, 5000, None, None) == 2
-    assert g(B(mx(8, 8192)), B(wb), 8, 5120, 8192, FAKE, 5124, None, None) == 3          # ldo*2 % 16
+    assert g(B(mx(8, 8192)), B(wb), 8, 5120, 8192, None, 5120, *W0, None, None) == 1
+    assert g(B(mx(8, 8192)), B(mx(5000, 8192)), 8, 5000, 8192, FAKE, 5000, *W0, None, None) == 2
+    assert g(B(mx(8, 8192)), B(wb), 8, 5120, 8192, FAKE, 5124, *W0, None, None) == 3          # ldo*2 % 16
+    assert g(B(mx(8, 8192)), B(wb), 8, 5120, 8192, FAKE, 5120, FAKE, 16, None, None) == 1     # workspace too small
     p = lib.o_proj_mxfp8
-    assert p(B(o), B(wa), B(wb), 8, 8, 1024, 4096, 5120, None, FAKE, None, None, FAKE, None, None) == 1
+    assert p(B(o), B(wa), B(wb), 8, 8, 1024, 4096, 5120, None, FAKE, None, None, FAKE, *W0, None, None) == 1
     assert p(B(o), B(wa), B(mx(5120, 8192, layout=1)), 8, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE,
-             None, None) == 4
+             *W0, None, None) == 4
+    assert p(B(o), B(wa), B(wb), 8, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, FAKE + 4, 1 << 30, None,
+             None) == 3                                                                      # misaligned workspace
 
 
 def test_o_proj_noalloc_argument_errors(lib):

@@ -66,6 +66,68 @@ def test_gemm_exact_integers(mxq, oracle, T, N, K):
                           f"got {bits_to_f64(got[tuple(bad[0])])} want {exact[tuple(bad[0])]}"
 
 
+# ------------------------------------------------------------------------------------------
+# stream-K split of the CTA-pair GEMM (T > 384 with a workspace)
+# ------------------------------------------------------------------------------------------
+def _flags_zero(mxq, ws):
+    """The flag bytes (after one 256 KB partial slot pair per SM pair) are all zero."""
+    per_pair = 2 * 128 * 1024 + 64
+    pairs = ws.numel() // per_pair
+    return bool((ws[pairs * 2 * 128 * 1024:] == 0).all())
+
+
+@pytest.mark.parametrize("T,N,K", [(1000, 5120, 8192), (2000, 5120, 8192)])
+def test_split_k_exact_integers(mxq, oracle, T, N, K):
+    """The split tail (80 and 160 tiles of 256 x 256 on the SM pairs, 64 k-blocks each: the last
+    wave and the remainder are cut into equal k-block ranges, and the pair that starts a tile adds
+    the partial sums of the others): with integer operands every partial sum is exact, so the
+    output equals the exact product bit for bit and the whole-tile (no workspace) result, and the
+    flags end at zero. T = 1000 also leaves the last tile's second CTA without tokens."""
+    rng = np.random.default_rng(T + N + K)
+    a = int_matrix(rng, T, K)
+    b = int_matrix(rng, N, K)
+    A, B = gpu_mx(mxq, a), gpu_mx(mxq, b)
+    ws = torch.zeros(mxq.workspace_bytes(), dtype=torch.uint8, device="cuda")
+    out = Guarded(T * N * 2)
+    mxq.gemm_mxfp8_bf16(A, B, out.view(torch.bfloat16, (T, N)), workspace=ws)
+    whole = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    mxq.gemm_mxfp8_bf16(A, B, whole, workspace=False)
+    torch.cuda.synchronize()
+    assert out.intact() and _flags_zero(mxq, ws)
+    pairs = ws.numel() // (2 * 128 * 1024 + 64)
+    assert bool((ws[: pairs * 2 * 128 * 1024] != 0).any())  # partial slots were written: the split ran
+    got = u8(out.body).view(np.uint16).reshape(T, N)
+    want = oracle.bf16_round(a.double().numpy() @ b.double().numpy().T)
+    assert np.array_equal(got, want)
+    assert np.array_equal(got, bf16_bits(whole))
+
+
+def test_split_k_o_proj_deterministic(mxq, weights):
+    """The pair at T = 1000 (wo_b split, wo_a in whole tiles) repeats its bytes exactly, stays
+    within one bf16 rounding of the whole-tile result, and leaves the flags zero."""
+    from mxfp8_activation_quant_gb300 import synth
+
+    T = 1000
+    O = gpu_mx(mxq, synth.o_proj_activation(3, T))
+    ws = torch.zeros(mxq.workspace_bytes(), dtype=torch.uint8, device="cuda")
+    res = []
+    for w in (ws, ws, False):
+        zq = torch.empty((T, synth.KB), dtype=torch.uint8, device="cuda")
+        ztl = mxq.empty_sf(mxq.SF_TILED_128X4, T, synth.KB, "cuda")
+        out = torch.empty((T, synth.NB), dtype=torch.bfloat16, device="cuda")
+        mxq.o_proj_mxfp8(O, weights.WA, weights.WB, T, synth.G, synth.NA, synth.KA, synth.NB, zq, ztl, out,
+                         workspace=w)
+        res.append((zq, ztl, out))
+    torch.cuda.synchronize()
+    assert _flags_zero(mxq, ws)
+    (zq1, ztl1, out1), (zq2, ztl2, out2), (_, _, out3) = res
+    assert torch.equal(zq1, zq2) and torch.equal(ztl1, ztl2) and torch.equal(out1, out2)
+    # only the fp32 summation order differs: a bf16 rounding step here and there
+    a, b = out1.float(), out3.float()
+    assert float((a - b).abs().max()) <= 2.0 ** -7 * float(b.abs().max())
+    assert float((a - b).norm()) <= 2e-3 * float(b.norm())
+
+
 @pytest.mark.parametrize("T", [5, 130, 260])
 def test_gemm_random_scales(mxq, oracle, T):
     from mxfp8_activation_quant_gb300 import synth
@@ -216,11 +278,11 @@ def test_o_proj_graph_replay(mxq, weights):
     ztl2 = torch.zeros_like(ztl)
     out2 = torch.zeros_like(out)
     s = torch.cuda.Stream()
-    with torch.cuda.stream(s):  # warm-up on a side stream before capture
+    with torch.cuda.stream(s):  # warm-up on the capture stream (it also makes its split workspace)
         mxq.o_proj_mxfp8(O, weights.WA, weights.WB, T, synth.G, synth.NA, synth.KA, synth.NB, zq2, ztl2, out2)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
+    with torch.cuda.graph(g, stream=s):
         mxq.o_proj_mxfp8(O, weights.WA, weights.WB, T, synth.G, synth.NA, synth.KA, synth.NB, zq2, ztl2, out2)
     zq2.zero_()
     ztl2.zero_()
