@@ -785,7 +785,9 @@ struct PairCfg {
 
 constexpr int kThreadsPair = 352;  // warp 0 TMA, 1 MMA, 2..9 epilogue, 10 scale copies
 
-template <int STAGES>
+// SK: the stream-K tail (p.sk_part / p.sk_flag set); a separate instantiation keeps the
+// whole-tile kernel's code exactly as without it
+template <int STAGES, bool SK>
 __global__ void __launch_bounds__(kThreadsPair, 1)
     gemm_mxf8_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __grid_constant__ CUtensorMap tm_b64, const __grid_constant__ CUtensorMap tm_sfa,
@@ -819,7 +821,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   // Work items, taken round robin by the pairs: the 256 x 256 tiles of the full waves, then, when
   // the last wave would leave more than half the pairs idle, its tiles as two 256 x 128 halves
   // each, which that wave spreads over twice as many pairs.
-  const bool sk = p.sk_part != nullptr;
+  constexpr bool sk = SK;
   const int tail = total % tile_step;
   const bool split_tail = !sk && tail > 0 && 2 * tail <= tile_step;
   const int n_items = split_tail ? total + tail : total;
@@ -1365,7 +1367,7 @@ int pair_clusters_resident() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_mxf8_pair<STAGES>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_mxf8_pair<STAGES, true>, &cfg) != cudaSuccess) {
       (void)cudaGetLastError();
       return 0;
     }
@@ -1378,9 +1380,12 @@ int pair_clusters_resident() {
 template <int STAGES>
 cudaError_t launch_pair(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   using C = PairCfg<STAGES>;
-  auto kern = gemm_mxf8_pair<STAGES>;
+  auto kern = gemm_mxf8_pair<STAGES, false>;
+  auto kern_sk = gemm_mxf8_pair<STAGES, true>;
   static const cudaError_t attr_err = set_smem_attrs(kern, C::SMEM_BYTES);
   if (attr_err != cudaSuccess) return attr_err;
+  static const cudaError_t attr_err_sk = set_smem_attrs(kern_sk, C::SMEM_BYTES);
+  if (attr_err_sk != cudaSuccess) return attr_err_sk;
   ka.splits = 1;
   ka.kb_per_cta = l.k_len / BK;
   const int64_t tiles = static_cast<int64_t>(l.G) * ceil_div(l.T, 2 * BM) * (l.n_feat / 256);
@@ -1409,6 +1414,7 @@ cudaError_t launch_pair(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
       ka.sk_part = reinterpret_cast<float4*>(ws);
       ka.sk_flag = reinterpret_cast<int32_t*>(ws + static_cast<int64_t>(max_pairs) * kSkSlotBytes);
       pairs = sk_pairs;
+      kern = kern_sk;
     }
   }
   CUtensorMap tma_act, tma_wt, tma_wt64, tma_sfa, tma_sfb;
