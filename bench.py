@@ -466,6 +466,25 @@ def sweep(args, mxq, synth, torch, dev, WA, WB):
                           "frac": round(roof / fused, 4),
                           "weight_GB/s": round(WEIGHT_BYTES / fused / 1e3, 1), **extra}), flush=True)
         del oq, osf, O, zq, zsf, zb, out
+    # The dense MXFP8 rate this library's own GEMM reaches on a square 8192^3 problem (random
+    # E4M3 operands), beside the two peaks the fractions could be taken against: the nominal
+    # dense fp8 figure and 2x the measured bf16 burst (the one the roofline lines use).
+    n = 8192
+    A = mxq.MXFP8(*_rand_mx(mxq, synth, n, n, synth.TID_SQ_A, dev))
+    B = mxq.MXFP8(*_rand_mx(mxq, synth, n, n, synth.TID_SQ_B, dev))
+    c = torch.empty((n, n), dtype=torch.bfloat16, device=dev)
+    us = timeit(lambda: mxq.gemm_mxfp8_bf16(A, B, c), reps=5)
+    tf = 2 * n ** 3 / us / 1e6
+    print(json.dumps({"sweep": "mxfp8_gemm_8192^3", "us": round(us, 2), "TFLOP/s": round(tf, 1),
+                      "frac_of_2x_measured_bf16": round(tf / mx_tf, 4), "frac_of_nominal_4500": round(tf / 4500.0, 4)}),
+          flush=True)
+
+
+def _rand_mx(mxq, synth, rows, cols, tid, dev):
+    """MXFP8 (bytes, F8_128x4 scales) of a seeded normal bf16 matrix, quantized by the library."""
+    x = synth.normal_bf16(0, tid, rows, cols, 1.0, device=dev)
+    q, sfs = mxq.quantize(x, layouts=(2,))
+    return q, sfs[2]
 
 
 # ---- the CPU oracle (cpu_baseline and the reference arm) -----------------------------------

@@ -42,6 +42,7 @@ TID_RMS_X = 20
 TID_RMS_GAMMA = 21
 TID_RMS_OUTLIER = 22
 TID_WQKV = 30
+TID_SQ_A, TID_SQ_B = 40, 41  # the square 8192^3 GEMM of the bench sweep
 
 # DeepSeek-V4.1 _o_proj shapes at TP1
 G, NA, KA, NB = 8, 1024, 4096, 5120
