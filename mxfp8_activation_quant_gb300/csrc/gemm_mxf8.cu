@@ -67,9 +67,10 @@ struct KArgs {
   int64_t z_mp4;
   int32_t* status;
   int64_t act_mp4;  // packed activation scales: rows per word column (ceil(T / 4) * 4)
-  // CTA-pair kernel, stream-K mode (null: round robin over whole tiles). Partial sums of the
-  // segments that do not start a tile: one 128 KB slot per CTA, [pair][rank][64 x 16-byte
-  // columns][128 rows]; ready flags [pair][rank][8 epilogue warps], zero between launches.
+  // CTA-pair kernel, split tail (the SK instantiation; null otherwise). Partial sums of the
+  // segments that do not start a tile: one 128 KB slot per CTA, [pair][rank][8 epilogue
+  // warps][32 x 16-byte column groups][32 lanes]; ready flags [pair][rank][8 epilogue warps],
+  // zero between launches.
   float4* sk_part;
   int32_t* sk_flag;
 };

@@ -68,13 +68,14 @@ struct GemmLaunch {
   // act_sf is MXQ_SF_PACKED_I32_MN (packed[w * Mp + m], Mp = ceil(T / 4) * 4). T <= 16 only.
   bool act_sf_packed;
   // Optional device workspace of at least split_workspace_bytes(), zero-filled before its first
-  // use and left zero-filled by every launch that completes: with it, the CTA-pair kernel splits
-  // the k-block iterations evenly over all pairs (stream-K); without it, pairs take whole tiles.
+  // use; every launch that completes leaves its flags zero. With it, the CTA-pair kernel may cut
+  // the k-block iterations of its last wave and remainder into equal ranges over all pairs
+  // (stream-K tail) when its cost model says that pays; without it, pairs take whole tiles.
   void* workspace;
   int64_t workspace_bytes;
 };
 cudaError_t launch_gemm(const GemmLaunch& a, cudaStream_t stream);
-// Workspace bytes the stream-K mode needs on the current device.
+// Workspace bytes the stream-K tail needs on the current device.
 int64_t split_workspace_bytes();
 
 }  // namespace mxq
