@@ -102,6 +102,42 @@ def test_split_k_exact_integers(mxq, oracle, T, N, K):
     assert np.array_equal(got, bf16_bits(whole))
 
 
+def test_split_k_grouped_fused_epilogue(mxq, oracle):
+    """The split tail under the fused z epilogue: a grouped einsum (G = 2, 2560 features, 8192
+    deep, T = 1000: 80 tiles) with integer operands gives bf16 z equal to the rounded exact
+    result, MXFP8 z equal to the standalone quantizer applied to that z, and the same bytes as
+    whole tiles."""
+    T, G, Na, Ka = 1000, 2, 2560, 8192
+    rng = np.random.default_rng(5)
+    o = int_matrix(rng, T, G * Ka, -3, 3)
+    wa = int_matrix(rng, G * Na, Ka, -3, 3)
+    O, WA = gpu_mx(mxq, o), gpu_mx(mxq, wa)
+    ws = torch.zeros(mxq.workspace_bytes(), dtype=torch.uint8, device="cuda")
+    outs = []
+    for w in (ws, False):
+        zq = Guarded(T * G * Na)
+        ztl = Guarded(mxq.sf_bytes(2, T, G * Na))
+        zb = Guarded(T * G * Na * 2)
+        mxq.wo_a_einsum_mxfp8(O, WA, T, G, Na, Ka, zq.view(shape=(T, G * Na)), ztl.body, None,
+                              zb.view(torch.bfloat16, (T, G * Na)), workspace=w)
+        outs.append((zq, ztl, zb))
+    torch.cuda.synchronize()
+    assert _flags_zero(mxq, ws)
+    pairs = ws.numel() // (2 * 128 * 1024 + 64)
+    assert bool((ws[: pairs * 2 * 128 * 1024] != 0).any())  # the split ran
+    (zq, ztl, zb), (zq_w, ztl_w, zb_w) = outs
+    for gbuf in (zq, ztl, zb, zq_w, ztl_w, zb_w):
+        assert gbuf.intact()
+    a, b = o.double().numpy(), wa.double().numpy()
+    exact = np.concatenate([a[:, g * Ka:(g + 1) * Ka] @ b[g * Na:(g + 1) * Na].T for g in range(G)], axis=1)
+    got = u8(zb.body).view(np.uint16).reshape(T, G * Na)
+    assert np.array_equal(got, oracle.bf16_round(exact))
+    q2, sfs = mxq.quantize(zb.view(torch.bfloat16, (T, G * Na)), layouts=(2,))
+    torch.cuda.synchronize()
+    assert torch.equal(q2, zq.view(shape=(T, G * Na))) and torch.equal(sfs[2], ztl.body)
+    assert torch.equal(zq.body, zq_w.body) and torch.equal(ztl.body, ztl_w.body) and torch.equal(zb.body, zb_w.body)
+
+
 def test_split_k_o_proj_deterministic(mxq, weights):
     """The pair at T = 1000 (wo_b split, wo_a in whole tiles) repeats its bytes exactly, stays
     within one bf16 rounding of the whole-tile result, and leaves the flags zero."""
