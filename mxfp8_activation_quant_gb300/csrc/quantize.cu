@@ -18,7 +18,7 @@ namespace mxq {
 namespace {
 
 constexpr int kUnits = 4;  // 256-column units per warp
-constexpr int kWarpsPerBlock = 8;
+constexpr int kWarpsPerBlock = 4;  // 128-thread blocks: about 1 % faster than 256 at every measured size
 constexpr int64_t kEarlyGammaRows = 256;  // RMSNorm row counts that load gamma early (measured)
 
 struct QuantArgs {
