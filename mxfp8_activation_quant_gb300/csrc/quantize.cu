@@ -50,7 +50,9 @@ __device__ __forceinline__ void store_unit_scales(const QuantArgs& a, int64_t ro
   }
 }
 
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) quantize_kernel(const QuantArgs a) {
+// at least 12 blocks per SM (40 registers): 75 % occupancy instead of 62.5 %, 1-2 % faster at
+// large sizes (16 blocks forces spills and is slower)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, 12) quantize_kernel(const QuantArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t wid = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
   const int64_t row = wid / a.chunks;
