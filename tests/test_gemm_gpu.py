@@ -45,7 +45,7 @@ def int_matrix(rng, rows, cols, lo=-4, hi=4):
 # ------------------------------------------------------------------------------------------
 # exact small GEMMs (both orientations, split and unsplit K, ragged token tails)
 # ------------------------------------------------------------------------------------------
-@pytest.mark.parametrize("T,N,K", [(1, 128, 128), (7, 128, 256), (16, 256, 512), (32, 128, 1024), (64, 128, 1024),
+@pytest.mark.parametrize("T,N,K", [(1, 128, 128), (1, 256, 1152), (2, 128, 640), (7, 128, 256), (16, 256, 512), (32, 128, 1024), (64, 128, 1024),
                                    (96, 128, 1024), (100, 128, 256), (128, 256, 2048), (200, 256, 1024),
                                    (250, 128, 1024), (256, 128, 512), (300, 256, 256), (384, 128, 384),
                                    (513, 256, 512)])
@@ -187,7 +187,7 @@ def test_gemm_random_scales(mxq, oracle, T):
 # ------------------------------------------------------------------------------------------
 # small grouped einsum: fused MXFP8 epilogue == standalone quantizer on the same bf16 z
 # ------------------------------------------------------------------------------------------
-@pytest.mark.parametrize("T", [1, 5, 129, 260])
+@pytest.mark.parametrize("T", [1, 2, 5, 129, 260])
 def test_wo_a_small_groups(mxq, oracle, T):
     from mxfp8_activation_quant_gb300 import synth
 
@@ -412,7 +412,7 @@ def test_o_proj_from_bf16_matches_prequantized(mxq, weights, T, pad):
         assert torch.equal(x, y)
 
 
-@pytest.mark.parametrize("T", [1, 5, 16])
+@pytest.mark.parametrize("T", [1, 2, 5, 16])
 def test_wo_b_reads_packed_scales(mxq, weights, T):
     """wo_b taking z with int32-packed MN-major scales (the layout the fused epilogue writes as
     its second output) gives the same bf16 output as with the F8_128x4 scales, standalone and as
