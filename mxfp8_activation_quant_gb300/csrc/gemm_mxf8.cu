@@ -131,7 +131,10 @@ struct Cfg {
   static constexpr int MAX_CO = 512 / TMEM_COLS;
   static constexpr int SMEM_FLOOR = SM_SMEM / (MAX_CO + 1) + 1024;
   static constexpr int SMEM_LAUNCH = SMEM_BYTES > SMEM_FLOOR ? SMEM_BYTES : SMEM_FLOOR;
-  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+  // Token (swap-AB) or feature tiles of 16..128 columns: the 128 x 256 tile of this kernel,
+  // with two B scale atoms, is not used (the CTA-pair kernel covers 256-wide tiles) and its
+  // scale and split-K paths are not validated.
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "MMA N");
   static_assert(TMEM_USED <= 512, "TMEM");
   // unsplit swap-AB epilogue: 128 features x (BN + 4) floats staged in the tile region
   static_assert(128 * (BN + 4) * 4 <= OFF_SF, "epilogue staging must fit in the tile region");
