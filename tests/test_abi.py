@@ -147,3 +147,27 @@ def test_selftest_argument_errors(lib):
     assert lib.mxq_selftest_wait_timeout(0, FAKE, None) == 1
     assert lib.mxq_selftest_wait_timeout(2000000, FAKE, None) == 1  # the limit stays within 1 s
     assert lib.mxq_selftest_wait_timeout(1000, FAKE + 4, None) == 3
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the built library every call raises; nothing falls back to another implementation."""
+    from mxfp8_activation_quant_gb300 import _lib
+
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "libmxq.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        _lib.abi_version()
+    with pytest.raises(RuntimeError, match="not built"):
+        _lib.workspace_bytes()
+
+
+def test_host_tensors_are_refused(lib):
+    """The binding passes device pointers only: a host tensor is an error, not a CPU path."""
+    import torch
+
+    from mxfp8_activation_quant_gb300 import _lib
+
+    x = torch.zeros(4, 32, dtype=torch.bfloat16)
+    q = torch.zeros(4, 32, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="device tensors"):
+        _lib.mxfp8_quantize(x, q)
