@@ -64,6 +64,13 @@ def wo_b_bytes(T):
     return NB * KB * 33 // 32 + T * KB * 33 // 32 + T * NB * 2
 
 
+def chain_config(T, world):
+    """The workload both arms report (the GPU arm's timing conditions included)."""
+    return {"workload": f"MXFP8 activation chain, DeepSeek-V4.1-Flash TP1 _o_proj + RMSNorm, T={T}",
+            "tokens": T, "wo_a": "8 groups x 4096 -> 1024", "wo_b": "8192 -> 5120", "rmsnorm_hidden": H,
+            "l2": "flushed before every step (outside the timed events)", "parallelism": f"replicas x{world}"}
+
+
 def wo_a_flops(T):
     return 2 * T * G * NA * KA
 
@@ -329,9 +336,7 @@ def run_gpu(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/ue8m0 (fp32 accum)",
         "data": "synthetic (seeded SplitMix64 + Box-Muller, shapes of the pages' workloads)",
-        "config": {"workload": f"MXFP8 activation chain, DeepSeek-V4.1-Flash TP1 _o_proj + RMSNorm, T={T}",
-                   "tokens": T, "wo_a": "8 groups x 4096 -> 1024", "wo_b": "8192 -> 5120", "rmsnorm_hidden": H,
-                   "l2": "flushed before every step (outside the timed events)", "parallelism": f"replicas x{world}"},
+        "config": chain_config(T, world),
         "parts": detail,
         "roofline": roof,
         "e2e": {"value": round(e2e_tps, 1), "unit": "tokens/s",
@@ -567,8 +572,7 @@ def run_reference(args):
     res = {"impl": "reference", "metric": METRIC, "value": round(tps, 3), "unit": "tokens/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-           "data": "synthetic", "config": {"workload": f"MXFP8 activation chain, DeepSeek-V4.1-Flash TP1 _o_proj + "
-                                                       f"RMSNorm, T={T}", "tokens": T},
+           "data": "synthetic", "config": chain_config(T, world),
            "cpu_baseline": {"value": round(tps, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
                             "kind": "oracle", "sample": sample},
            "e2e": {"value": round(tps, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
