@@ -263,7 +263,7 @@ def run_o_proj(mxq, w, O, T, with_bf16=True):
     return zq, ztl, zb, out
 
 
-@pytest.mark.parametrize("T", [1, 2, 4, 7, 8, 16, 64, 128, 129, 256, 300, 384])
+@pytest.mark.parametrize("T", [1, 2, 4, 7, 8, 16, 24, 33, 64, 100, 128, 129, 256, 300, 384])
 def test_o_proj_decode_shapes(mxq, oracle, weights, T):
     from mxfp8_activation_quant_gb300 import synth
 
@@ -281,7 +281,7 @@ def test_o_proj_decode_shapes(mxq, oracle, weights, T):
     assert torch.equal(zq2, zq) and torch.equal(ztl2, ztl) and torch.equal(out2, out)
 
 
-@pytest.mark.parametrize("T", [512, 4096, 8193, 32768])
+@pytest.mark.parametrize("T", [385, 512, 1000, 4096, 8193, 32768])
 def test_o_proj_prefill_sampled_rows(mxq, oracle, weights, T):
     """Full-size prefill: the oracle checks the first and last 128-row tiles and 256 seeded
     rows; the fused-vs-standalone identity is checked on every row."""
