@@ -48,7 +48,10 @@ def int_matrix(rng, rows, cols, lo=-4, hi=4):
 @pytest.mark.parametrize("T,N,K", [(1, 128, 128), (1, 256, 1152), (2, 128, 640), (7, 128, 256), (16, 256, 512), (32, 128, 1024), (64, 128, 1024),
                                    (96, 128, 1024), (100, 128, 256), (128, 256, 2048), (200, 256, 1024),
                                    (250, 128, 1024), (256, 128, 512), (300, 256, 256), (384, 128, 384),
-                                   (513, 256, 512)])
+                                   (513, 256, 512),
+                                   # wo_b's shape at three token bands, and 65 k-blocks (no power of
+                                   # two divides them: K stays unsplit)
+                                   (33, 5120, 8192), (100, 5120, 8192), (64, 5120, 8320)])
 def test_gemm_exact_integers(mxq, oracle, T, N, K):
     rng = np.random.default_rng(T * 7 + N + K)
     a = int_matrix(rng, T, K)
