@@ -150,6 +150,14 @@ __device__ __forceinline__ int recv_swizzle(int row, int cpr) {
   return cpr >= 8 ? (row & 7) : ((row * cpr) >> 3) & (cpr - 1);
 }
 
+// An uneven split of n items (k-blocks, or 4-column chunks of the token tile) over US ranks:
+// rank o takes [us_lo(o), us_lo(o + 1)).
+template <int US>
+__host__ __device__ constexpr int us_lo(int o, int n) { return o * n / (US > 0 ? US : 1); }
+// the rank that owns item x
+template <int US>
+__host__ __device__ constexpr int us_owner(int x, int n) { return ((x + 1) * US + n - 1) / n - 1; }
+
 __device__ __forceinline__ uint32_t amax_bf16x2_words(const uint32_t* hb, int n) {
   uint32_t m = 0;
 #pragma unroll
@@ -265,11 +273,14 @@ __device__ __forceinline__ void epi_token_group(const KArgs& p, const float (&v)
   }
 }
 
-template <int BN, int STAGES, bool SWAP, int ACT = kActMx>
+// US > 0: the swap-AB wide-tile kernel with K split over US cluster ranks, a count that need
+// not divide the k-blocks or the token columns (p.kb_per_cta then holds all k-blocks of K).
+template <int BN, int STAGES, bool SWAP, int ACT = kActMx, int US = 0>
 __global__ void __launch_bounds__(kThreads, 3)
     gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                      const KArgs p) {
   static_assert(ACT == kActMx || (SWAP && BN == 16), "converted activations: decode tiles only");
+  static_assert(US == 0 || (SWAP && ACT == kActMx && BN >= 32 && US <= BN / 4), "uneven split: wide tiles");
   constexpr bool CVT = ACT != kActMx;  // a staged activation part converted by the epilogue warps
   using C = Cfg<BN, STAGES, ACT>;
   extern __shared__ uint8_t smem_raw[];
@@ -328,8 +339,8 @@ __global__ void __launch_bounds__(kThreads, 3)
     b_rt0 = b_row0 >> 7;
     b_kc0 = 0;
   }
-  const int kb_begin = split * p.kb_per_cta;
-  const int nk = p.kb_per_cta;
+  const int kb_begin = US > 0 ? us_lo<US>(split, p.kb_per_cta) : split * p.kb_per_cta;
+  const int nk = US > 0 ? us_lo<US>(split + 1, p.kb_per_cta) - kb_begin : p.kb_per_cta;
   const int pre = nk < STAGES ? nk : STAGES;  // stages that need no free-slot wait
 
   const uint32_t a_dst0 = sbase, b_dst0 = sbase + C::OFF_B, sf_dst0 = sbase + C::OFF_SF;
@@ -388,7 +399,9 @@ __global__ void __launch_bounds__(kThreads, 3)
       mbar_init(bar_recv, 1);
       // PUSH: every rank, this one included, sends 128 features x (BN / splits) columns of fp32;
       // otherwise each other rank sends one block of that size
-      mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>(C::PUSH ? 128 * BN * 4 : 128 * BN * 4 / p.splits * (p.splits - 1)));
+      mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>(C::PUSH ? 128 * BN * 4
+                                                            : US > 0 ? 2048 * (us_lo<US>(split + 1, BN / 4) - us_lo<US>(split, BN / 4)) * (US - 1)
+                                                                     : 128 * BN * 4 / p.splits * (p.splits - 1)));
     }
     *abort_flag = 0;
     *issued_cnt = 0;
@@ -613,6 +626,95 @@ __global__ void __launch_bounds__(kThreads, 3)
         }
       }
     }
+  } else if (US > 0 && recv_path) {
+    if constexpr (US > 0) {
+    // The same exchange for an uneven split (US ranks): rank o owns the 4-column chunks
+    // [us_lo(o), us_lo(o + 1)) of the token tile; the staged blocks lie in chunk order, owner o's
+    // at 2 KB x us_lo(o). Chunk ownership is resolved at compile time in the fully unrolled
+    // staging loop; odd chunk counts per row need no swizzle (8 consecutive rows already fall on
+    // 8 different 16-byte bank positions).
+    constexpr int NCH = BN / 4;
+    const uint32_t rank = cluster_ctarank();
+    const int own_lo = us_lo<US>(static_cast<int>(rank), NCH);
+    const int own_cpr = us_lo<US>(static_cast<int>(rank) + 1, NCH) - own_lo;
+    const int own_cols = 4 * own_cpr;
+    const uint32_t own_blk = static_cast<uint32_t>(2048 * own_cpr);
+    const uint32_t stage0 = sbase;            // this rank's partial: every owner's block
+    const uint32_t recv0 = sbase + BN * 512;  // US - 1 blocks of this rank's columns
+    const int f = 32 * q + lane;
+    if (epi && !__any_sync(0xffffffffu, *abort_flag)) {
+#pragma unroll
+      for (int c = 0; c < BN / 16; ++c) {
+        uint32_t acc[16];
+        tmem_ld_x16(t_lane + 16 * c, acc);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int x = 4 * c + k;
+          const int lo = us_lo<US>(us_owner<US>(x, NCH), NCH);
+          const int cpr = us_lo<US>(us_owner<US>(x, NCH) + 1, NCH) - lo;
+          const int chunk = (cpr & (cpr - 1)) == 0 ? (x - lo) ^ recv_swizzle(f, cpr) : x - lo;
+          st_smem_v4(stage0 + static_cast<uint32_t>(2048 * lo + (f * cpr + chunk) * 16), acc[4 * k], acc[4 * k + 1],
+                     acc[4 * k + 2], acc[4 * k + 3]);
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    cluster_arrive();
+    cluster_wait();
+    if (threadIdx.x == 64 && !*abort_flag) {
+      for (int d = 1; d < US; ++d) {
+        const int o = (static_cast<int>(rank) + d) % US;
+        const int slot = (static_cast<int>(rank) + US - o - 1) % US;  // this rank among o's sources
+        const int lo = us_lo<US>(o, NCH);
+        const uint32_t blk = static_cast<uint32_t>(2048 * (us_lo<US>(o + 1, NCH) - lo));
+        bulk_s2s(mapa_shared(recv0 + slot * blk, static_cast<uint32_t>(o)), stage0 + static_cast<uint32_t>(2048 * lo), blk,
+                 mapa_shared(bar_recv, static_cast<uint32_t>(o)));
+      }
+    }
+    if (epi) {
+      if (!mbar_wait_bounded(bar_recv, 0)) {
+        *abort_flag = 1;
+        report_timeout(p.status);
+      }
+    }
+    __syncwarp();
+    cluster_arrive();
+    if (epi && !__any_sync(0xffffffffu, *abort_flag)) {
+      const float* sm = reinterpret_cast<const float*>(smem);
+      const bool pow2 = (own_cpr & (own_cpr - 1)) == 0;
+      // own_cols takes one of two values, so the division by it is one by a constant
+      constexpr int kColsLo = 4 * (NCH / US), kColsHi = 4 * ((NCH + US - 1) / US);
+      for (int w = static_cast<int>(threadIdx.x) - 64; w < 4 * own_cols; w += 128) {
+        const int gq = own_cols == kColsLo ? w / kColsLo : w / kColsHi;
+        const int j = w - gq * own_cols;
+        const int64_t t = b_row0 + 4 * own_lo + j;
+        const int64_t col = static_cast<int64_t>(g) * p.n_feat + m0 + 32 * gq;
+        if (t >= p.T) {  // padding token: only its zero scale is stored
+          epi_zero_scale(p, t, col);
+          continue;
+        }
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        for (int r = 0; r < US; ++r) {
+          const uint32_t base = r == static_cast<int>(rank)
+                                    ? stage0 + static_cast<uint32_t>(2048 * own_lo)
+                                    : recv0 + static_cast<uint32_t>((r + US - static_cast<int>(rank) - 1) % US) * own_blk;
+          const float* blkp = sm + (base - sbase) / 4;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int row = 32 * gq + i;
+            const int ch = pow2 ? (j >> 2) ^ recv_swizzle(row, own_cpr) : j >> 2;
+            const float x = blkp[row * own_cols + 4 * ch + (j & 3)];
+            v[i] = r == 0 ? x : v[i] + x;
+          }
+        }
+        epi_token_group(p, v, t, col);
+      }
+    }
+    }  // if constexpr (US > 0)
   } else if (recv_path) {
     // K split over the cluster; rank o owns the token columns [o*per_rank, (o+1)*per_rank).
     // Every rank stages its fp32 partial in its own shared memory, one block per owner laid out
@@ -1277,10 +1379,10 @@ int ctas_per_sm() {
   return by_smem < by_tmem ? by_smem : by_tmem;
 }
 
-template <int BN, int STAGES, bool SWAP, int ACT = kActMx>
+template <int BN, int STAGES, bool SWAP, int ACT = kActMx, int US = 0>
 cudaError_t launch_cfg(const GemmLaunch& l, const KArgs& ka, dim3 grid, int cluster_z, cudaStream_t stream) {
   using C = Cfg<BN, STAGES, ACT>;
-  auto kern = gemm_mxf8_kernel<BN, STAGES, SWAP, ACT>;
+  auto kern = gemm_mxf8_kernel<BN, STAGES, SWAP, ACT, US>;
   static const cudaError_t attr_err = set_smem_attrs(kern, C::SMEM_LAUNCH);
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap tma_act, tma_wt;
@@ -1325,6 +1427,34 @@ int pick_splits(int tiles, int kb_total, int slots) {
   return 1;
 }
 
+// Clusters of US CTAs of the uneven-split swap-AB kernel that fit on the device at once.
+template <int BN, int STAGES, int US>
+int uneven_clusters_resident() {
+  static const int n = [] {
+    using C = Cfg<BN, STAGES, kActMx>;
+    auto kern = gemm_mxf8_kernel<BN, STAGES, true, kActMx, US>;
+    if (set_smem_attrs(kern, C::SMEM_LAUNCH) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, static_cast<unsigned>(8 * US));
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_LAUNCH;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = static_cast<unsigned>(US);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return 0;
+    }
+    return clusters;
+  }();
+  return n;
+}
+
 template <int BN, int STAGES, int ACT = kActMx>
 cudaError_t launch_swap(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   const int tok_tiles = static_cast<int>(ceil_div(l.T, BN));
@@ -1332,6 +1462,20 @@ cudaError_t launch_swap(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   const int kb_total = l.k_len / BK;
   const int slots = num_sms() * ctas_per_sm<BN, STAGES, ACT>();
   const int s = pick_splits<BN, STAGES, ACT>(tiles, kb_total, slots);
+  // The one-CTA-per-SM band (128-token tiles, 6 stages): when the power-of-two split leaves SMs
+  // idle (wo_b at T <= 128: 40 tiles x 2 ranks on 152 SMs), 3 ranks fill more of them (120 CTAs).
+  if constexpr (BN == 128 && STAGES == 6 && ACT == kActMx) {
+    constexpr int US = 3;
+    constexpr bool fits = BN * 512 + 2048 * ((BN / 4 + US - 1) / US) * (US - 1) <= Cfg<BN, STAGES, ACT>::OFF_SF;
+    if (fits && s < US && tiles * s < num_sms() && tiles * US <= slots && kb_total >= 2 * US &&
+        tiles <= uneven_clusters_resident<BN, STAGES, US>()) {
+      ka.splits = US;
+      ka.kb_per_cta = kb_total;  // all k-blocks: the kernel cuts the uneven ranges
+      ka.per_rank_shift = 0;
+      dim3 grid(static_cast<unsigned>(l.n_feat / BM), static_cast<unsigned>(tok_tiles), static_cast<unsigned>(l.G * US));
+      return launch_cfg<BN, STAGES, true, ACT, US>(l, ka, grid, US, stream);
+    }
+  }
   ka.splits = s;
   ka.kb_per_cta = kb_total / s;
   ka.per_rank_shift = 0;
