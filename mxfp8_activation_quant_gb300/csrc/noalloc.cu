@@ -51,7 +51,8 @@ mxq_status o_proj_mxfp8_noalloc(const mxq_mx_tensor* o, const mxq_mx_tensor* wa,
   const mxq_status st = mxq::from_cuda(scratch_for_current_device(&base));
   if (st != MXQ_OK) return st;
   unsigned char* z_q = static_cast<unsigned char*>(base);
-  // T <= 256 here: the GEMMs never take the split path, so no workspace
+  // No split workspace: at any T the buffer admits (T <= 256 at G * Na = 8192, up to 2048 with
+  // G * Na = 1024) the large-T CTA-pair kernel then runs whole tiles, which needs none.
   return o_proj_mxfp8(o, wa, wb, T, G, Na, Ka, Nb, z_q, z_q + MXQ_NOALLOC_Z_BYTES, nullptr, nullptr, out_bf16, nullptr, 0,
                       status, stream);
 }

@@ -11,6 +11,7 @@ Overview / Validation / Details).
 Token counts follow the pages' tests: 1, 129, 8193 tokens and M in {1, 4, 7, 64, 300}, plus the
 decode and prefill sweeps."""
 import ctypes
+import re
 
 import numpy as np
 import pytest
@@ -49,6 +50,9 @@ def int_matrix(rng, rows, cols, lo=-4, hi=4):
                                    (96, 128, 1024), (100, 128, 256), (128, 256, 2048), (200, 256, 1024),
                                    (250, 128, 1024), (256, 128, 512), (300, 256, 256), (384, 128, 384),
                                    (513, 256, 512),
+                                   # more than 384 tokens with N % 256 != 0: the one-CTA
+                                   # normal-orientation kernel (128 tokens x 128 features per tile)
+                                   (513, 384, 512), (1000, 640, 1024), (8193, 128, 256),
                                    # wo_b's shape at three token bands, and 65 k-blocks (no power of
                                    # two divides them: K stays unsplit)
                                    (33, 5120, 8192), (100, 5120, 8192), (64, 5120, 8320)])
@@ -219,6 +223,73 @@ def test_wo_a_small_groups(mxq, oracle, T):
     assert torch.equal(sfs[2], ztl.body) and torch.equal(sfs[1], zpk.body)
 
 
+def test_wo_a_grouped_normal_orientation(mxq, oracle):
+    """A grouped einsum whose feature count per group is not a multiple of 256 (G = 2, Na = 384)
+    with more than 384 tokens runs on the one-CTA normal-orientation kernel. Integer operands make
+    every sum exact: the bf16 z equals the rounded exact product bit for bit, and the fused MXFP8
+    z and both its scale layouts equal the standalone quantizer applied to that z."""
+    T, G, Na, Ka = 700, 2, 384, 512
+    rng = np.random.default_rng(17)
+    o = int_matrix(rng, T, G * Ka, -3, 3)
+    wa = int_matrix(rng, G * Na, Ka, -3, 3)
+    O, WA = gpu_mx(mxq, o), gpu_mx(mxq, wa)
+    zq = Guarded(T * G * Na)
+    ztl = Guarded(mxq.sf_bytes(2, T, G * Na))
+    zpk = Guarded(mxq.sf_bytes(1, T, G * Na))
+    zb = Guarded(T * G * Na * 2)
+    mxq.wo_a_einsum_mxfp8(O, WA, T, G, Na, Ka, zq.view(shape=(T, G * Na)), ztl.body, zpk.body,
+                          zb.view(torch.bfloat16, (T, G * Na)))
+    torch.cuda.synchronize()
+    for gbuf in (zq, ztl, zpk, zb):
+        assert gbuf.intact()
+    a, b = o.double().numpy(), wa.double().numpy()
+    exact = np.concatenate([a[:, g * Ka:(g + 1) * Ka] @ b[g * Na:(g + 1) * Na].T for g in range(G)], axis=1)
+    got = u8(zb.body).view(np.uint16).reshape(T, G * Na)
+    assert np.array_equal(got, oracle.bf16_round(exact))
+    q2, sfs = mxq.quantize(zb.view(torch.bfloat16, (T, G * Na)), layouts=(1, 2))
+    torch.cuda.synchronize()
+    assert torch.equal(q2, zq.view(shape=(T, G * Na)))
+    assert torch.equal(sfs[2], ztl.body) and torch.equal(sfs[1], zpk.body)
+    # and the oracle's quantizer on the oracle's own rounded product gives the same bytes
+    oq, osf = oracle.quantize_bf16(oracle.bf16_round(exact))
+    assert np.array_equal(u8(zq.body).reshape(T, G * Na), oq)
+    assert np.array_equal(oracle.sf_from_128x4(u8(ztl.body), T, G * Na // 32), osf)
+
+
+def launched_kernels(fn):
+    """Names of the device kernels `fn` launches (torch.profiler / CUPTI); None when the
+    profiler records no kernels at all in this environment."""
+    from torch.profiler import ProfilerActivity, profile
+
+    torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        fn()
+        torch.cuda.synchronize()
+    names = [e.name for e in prof.events() if "cuda" in str(getattr(e, "device_type", "")).lower()]
+    return names or None
+
+
+@pytest.mark.parametrize("T", [100, 128])
+def test_uneven_split_kernel_runs_at_wo_b_shape(mxq, oracle, T):
+    """wo_b's shape in the 64 < T <= 128 band takes the swap-AB kernel with K cut over three
+    cluster ranks (the power-of-two split would leave SMs idle); check that this instantiation is
+    the one that ran, and that its integer-operand output is exact."""
+    N, K = 5120, 8192
+    rng = np.random.default_rng(T + 3)
+    a = int_matrix(rng, T, K)
+    b = int_matrix(rng, N, K)
+    A, B = gpu_mx(mxq, a), gpu_mx(mxq, b)
+    out = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    names = launched_kernels(lambda: mxq.gemm_mxfp8_bf16(A, B, out))
+    if names is None:
+        pytest.skip("the profiler records no device kernels here")
+    gemm = [n for n in names if "gemm_mxf8" in n]
+    assert len(gemm) == 1, names
+    assert re.search(r"gemm_mxf8_kernel<128, 6, (true|1), 0, 3>", gemm[0]), gemm[0]
+    want = oracle.bf16_round(a.double().numpy() @ b.double().numpy().T)
+    assert np.array_equal(bf16_bits(out), want)
+
+
 # ------------------------------------------------------------------------------------------
 # full DeepSeek-V4.1 _o_proj shapes
 # ------------------------------------------------------------------------------------------
@@ -385,11 +456,12 @@ def test_fused_chain_launches_two_kernels(mxq, weights, T):
     assert _kernel_nodes(g2) == (3, 3)
 
 
-@pytest.mark.parametrize("T,pad", [(1, 0), (2, 0), (7, 64), (16, 0)])
-def test_o_proj_from_bf16_matches_prequantized(mxq, weights, T, pad):
+@pytest.mark.parametrize("T,pad", [(1, 0), (2, 0), (4, 0), (7, 64), (16, 0)])
+def test_o_proj_from_bf16_matches_prequantized(mxq, oracle, weights, T, pad):
     """wo_a quantizing bf16 o in the kernel gives the same bytes as mxfp8_quantize(o) followed
     by o_proj_mxfp8: z, both scale layouts, the bf16 z and out (the pages' "pre-quantized ==
-    in-kernel"). `pad` extra columns make o a strided view."""
+    in-kernel"); and the in-kernel path on its own meets the oracle chain's tolerances (bf16 z
+    within 4e-3, out within 1e-2). `pad` extra columns make o a strided view."""
     from mxfp8_activation_quant_gb300 import synth
 
     o_full = torch.zeros((T, synth.G * synth.KA + pad), dtype=torch.bfloat16, device="cuda")
@@ -413,13 +485,19 @@ def test_o_proj_from_bf16_matches_prequantized(mxq, weights, T, pad):
     mxq.check_status(st)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+    z_ref, out_ref = oracle_chain(oracle, weights, bf16_bits(o))
+    assert rel_fro(bits_to_f64(bf16_bits(a[3])), z_ref) <= 4e-3
+    assert rel_fro(bits_to_f64(bf16_bits(a[4])), out_ref) <= 1e-2
 
 
 @pytest.mark.parametrize("T", [1, 2, 5, 16])
-def test_wo_b_reads_packed_scales(mxq, weights, T):
+def test_wo_b_reads_packed_scales(mxq, oracle, weights, T):
     """wo_b taking z with int32-packed MN-major scales (the layout the fused epilogue writes as
     its second output) gives the same bf16 output as with the F8_128x4 scales, standalone and as
-    the dependent half of the pair."""
+    the dependent half of the pair. Against the oracle: the packed words decode (oracle's
+    definition of the layout) to the same scales as the tiled ones; the output equals the fp64
+    GEMM on this z's bytes and decoded packed scales within one bf16 rounding plus fp32
+    summation error; and the chain output is within 1e-2 of the oracle's own chain."""
     from mxfp8_activation_quant_gb300 import synth
 
     O = gpu_mx(mxq, synth.o_proj_activation(9, T))
@@ -436,6 +514,16 @@ def test_wo_b_reads_packed_scales(mxq, weights, T):
     assert torch.equal(out_pk, out_tl)
     # the standalone wo_b (5 stages) splits K like the paired one: same bytes as the pair too
     assert torch.equal(out_pk, out)
+    Kg = synth.KB // 32
+    sf_pk = oracle.sf_unpack_i32(u8(zpk).view(np.uint32).reshape(Kg // 4, -1), T, Kg)
+    assert np.array_equal(sf_pk, oracle.sf_from_128x4(u8(ztl), T, Kg))
+    zd = oracle.dequant(u8(zq), sf_pk)
+    ref = oracle.gemm_nt(zd, weights.wb_d)
+    scale = oracle.gemm_nt(np.abs(zd), np.abs(weights.wb_d))
+    got = bits_to_f64(bf16_bits(out_pk))
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + scale * synth.KB * 2.0 ** -23 + 1e-30)
+    _, out_ref = oracle_chain(oracle, weights, bf16_bits(synth.o_proj_activation(9, T)))
+    assert rel_fro(got, out_ref) <= 1e-2
     if T == 16:
         big = mxq.MXFP8(torch.zeros((17, synth.KB), dtype=torch.uint8, device="cuda"),
                         mxq.empty_sf(1, 17, synth.KB), mxq.SF_PACKED_I32_MN)
