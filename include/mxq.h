@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define MXQ_ABI_VERSION 2
+#define MXQ_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define MXQ_API __attribute__((visibility("default")))
@@ -144,18 +144,26 @@ MXQ_API mxq_status rmsnorm_dual_out(const void* x_bf16, const void* gamma_bf16, 
 /*
  * Split workspace of the large-T GEMMs (T > 384). With more than 384 tokens the GEMMs run as
  * 256 x 256 tiles on pairs of SMs; when the tile count is not a multiple of the pairs, the last
- * wave would leave pairs idle. Given a workspace, the k-block iterations of all tiles are instead
- * divided evenly over the pairs, and a pair that starts a tile adds the fp32 partial sums of the
- * pairs that hold its later k-blocks (in k order: the result does not depend on timing, but may
- * differ from the no-workspace result in the last bit of a rounding).
+ * wave would leave pairs idle. Given a workspace, the k-block iterations of the last wave and the
+ * remainder are instead divided evenly over the pairs. At most two pairs then share a tile: each
+ * takes an arrival ticket when its MMAs are done, the first stores its fp32 partial sums in the
+ * workspace, and the second adds them to its own and writes the outputs. The result does not
+ * depend on timing or on which pair finishes, but may differ from the no-workspace result in the
+ * last bit of a rounding.
  *
- * mxq_workspace_bytes() is the size for the current device (two 128 KB fp32 partial slots and
- * 64 bytes of flags per SM pair, the flags last). The caller owns the buffer (16-byte aligned).
- * It must be zero-filled before its first use; every call that completes leaves its flags zero
- * again, so it needs no clearing between calls (after a call that reported MXQ_ERR_TIMEOUT, zero
- * it again). Calls that overlap in time
- * (different streams) need separate workspaces; calls ordered on one stream may share one,
- * including both GEMMs of o_proj_mxfp8. NULL workspace: whole tiles per pair, no partials.
+ * Forward progress: no pair ever waits for a pair that has not started (the finisher waits only
+ * for a sharer that already holds its ticket and is storing). So a split call completes however
+ * few SMs are free for it -- kernels on other streams, an MPS or green-context SM limit -- it
+ * only runs slower.
+ *
+ * mxq_workspace_bytes() is the size for the current device: per SM pair, four 128 KB fp32
+ * partial slots (a pair's first and last segment, both CTAs), then 128 bytes of ready flags and
+ * 128 bytes of tickets for all pairs (flags and tickets last). The caller owns the buffer
+ * (16-byte aligned). It must be zero-filled before its first use; every call that completes
+ * leaves its flags and tickets zero again, so it needs no clearing between calls (after a call
+ * that reported MXQ_ERR_TIMEOUT, zero it again). Calls that overlap in time (different streams)
+ * need separate workspaces; calls ordered on one stream may share one, including both GEMMs of
+ * o_proj_mxfp8. NULL workspace: whole tiles per pair, no partials.
  */
 MXQ_API int64_t mxq_workspace_bytes(void);
 
@@ -220,6 +228,15 @@ MXQ_API mxq_status o_proj_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa,
  * diagnostic of this library. status: a zeroed status word (required).
  */
 MXQ_API mxq_status mxq_selftest_wait_timeout(int64_t limit_us, void* status, void* stream);
+
+/*
+ * mxq_selftest_hold_sms -- a diagnostic of this library (no page describes it): occupies
+ * `sm_pairs` pairs of SMs (clusters of two CTAs, each with enough shared memory that no GEMM CTA
+ * of this library fits beside it) for hold_us microseconds (1..2,000,000), then returns. Every
+ * wait in it is on the clock, so it always ends. Used to check that calls complete while other
+ * work holds SMs. Requires 1 <= sm_pairs <= the device's SMs / 2.
+ */
+MXQ_API mxq_status mxq_selftest_hold_sms(int64_t sm_pairs, int64_t hold_us, void* stream);
 
 /*
  * o_proj_mxfp8_from_bf16 -- the _o_proj pair at decode sizes (T <= 16) fed by bf16 o

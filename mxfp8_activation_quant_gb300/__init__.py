@@ -19,6 +19,7 @@ from ._lib import (  # noqa: F401
     o_proj_mxfp8_noalloc,
     quantize,
     rmsnorm_dual_out,
+    selftest_hold_sms,
     selftest_wait_timeout,
     sf_bytes,
     status_bytes,

@@ -54,6 +54,7 @@ SIGNATURES = {
     "mxq_status_bytes": ([], ctypes.c_size_t),
     "mxq_check_status": ([P, P], ctypes.c_int),
     "mxq_selftest_wait_timeout": ([I64, P, P], ctypes.c_int),
+    "mxq_selftest_hold_sms": ([I64, I64, P], ctypes.c_int),
     "mxfp8_quantize": ([P, I64, I64, I64, P, I64, P, P, P, P], ctypes.c_int),
     "rmsnorm_dual_out": ([P, P, ctypes.c_float, I64, I64, I64, P, P, P, P, P, P], ctypes.c_int),
     "mxq_workspace_bytes": ([], I64),
@@ -261,3 +262,8 @@ def o_proj_mxfp8_from_bf16(o: torch.Tensor, wa: MXFP8, wb: MXFP8, T: int, G: int
 def selftest_wait_timeout(limit_us: int, status: torch.Tensor, stream=None) -> None:
     """Launch the bounded-wait self-test: a wait that runs out after limit_us and reports a timeout."""
     _check(load().mxq_selftest_wait_timeout(limit_us, _ptr(status), _stream(stream)), "mxq_selftest_wait_timeout")
+
+
+def selftest_hold_sms(sm_pairs: int, hold_us: int, stream=None) -> None:
+    """Occupy `sm_pairs` SM pairs for hold_us microseconds (a clock-bounded diagnostic kernel)."""
+    _check(load().mxq_selftest_hold_sms(sm_pairs, hold_us, _stream(stream)), "mxq_selftest_hold_sms")

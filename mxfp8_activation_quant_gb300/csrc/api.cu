@@ -24,6 +24,18 @@ __global__ void selftest_wait_kernel(uint64_t limit_ns, int32_t* status) {
     if (!mxq::mbar_wait_limit(b, 0, limit_ns) && status != nullptr) atomicCAS(status, 0, MXQ_ERR_TIMEOUT);
   }
 }
+
+// Holds an SM for hold_ns: a CTA whose shared memory leaves no room for a GEMM CTA of this
+// library beside it, one thread watching the clock (the wait always ends).
+constexpr int kHoldSmemBytes = 160 * 1024;
+__global__ void selftest_hold_kernel(uint64_t hold_ns) {
+  extern __shared__ uint8_t hold_smem[];
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = mxq::globaltimer_ns();
+    while (mxq::globaltimer_ns() - t0 < hold_ns) __nanosleep(2000);
+    hold_smem[0] = 0;
+  }
+}
 }  // namespace
 
 mxq_status mxq::from_cuda(cudaError_t e) {
@@ -318,6 +330,30 @@ mxq_status mxq_selftest_wait_timeout(int64_t limit_us, void* status, void* strea
   selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint64_t>(limit_us) * 1000u,
                                                                       static_cast<int32_t*>(status));
   return from_cuda(cudaGetLastError());
+}
+
+mxq_status mxq_selftest_hold_sms(int64_t sm_pairs, int64_t hold_us, void* stream) {
+  int dev = 0, sms = 0;
+  mxq_status st = from_cuda(cudaGetDevice(&dev));
+  if (st == MXQ_OK) st = from_cuda(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  if (st != MXQ_OK) return st;
+  if (sm_pairs < 1 || sm_pairs > sms / 2 || hold_us < 1 || hold_us > 2000000) return MXQ_ERR_INVALID_ARG;
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(selftest_hold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kHoldSmemBytes);
+  if (attr != cudaSuccess) return from_cuda(attr);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * sm_pairs), 1, 1);
+  cfg.blockDim = dim3(32, 1, 1);
+  cfg.dynamicSmemBytes = kHoldSmemBytes;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute a[1];
+  a[0].id = cudaLaunchAttributeClusterDimension;  // whole SM pairs, as the CTA-pair GEMM uses them
+  a[0].val.clusterDim.x = 2;
+  a[0].val.clusterDim.y = 1;
+  a[0].val.clusterDim.z = 1;
+  cfg.attrs = a;
+  cfg.numAttrs = 1;
+  return from_cuda(cudaLaunchKernelEx(&cfg, selftest_hold_kernel, static_cast<uint64_t>(hold_us) * 1000u));
 }
 
 }  // extern "C"

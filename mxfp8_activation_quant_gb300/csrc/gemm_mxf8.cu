@@ -68,11 +68,13 @@ struct KArgs {
   int32_t* status;
   int64_t act_mp4;  // packed activation scales: rows per word column (ceil(T / 4) * 4)
   // CTA-pair kernel, split tail (the SK instantiation; null otherwise). Partial sums of the
-  // segments that do not start a tile: one 128 KB slot per CTA, [pair][rank][8 epilogue
-  // warps][32 x 16-byte column groups][32 lanes]; ready flags [pair][rank][8 epilogue warps],
-  // zero between launches.
+  // sharers of a split tile that do not finish it: two 128 KB slots per CTA (a pair's first and
+  // last segment), [pair][segment][rank][8 epilogue warps][32 x 16-byte column groups][32 lanes];
+  // ready flags [pair][segment][rank][8 epilogue warps]; arrival tickets [tail tile][rank][8
+  // epilogue warps]. Flags and tickets are zero between launches.
   float4* sk_part;
   int32_t* sk_flag;
+  int32_t* sk_ticket;
 };
 
 __device__ __forceinline__ void report_timeout(int32_t* status) {
@@ -891,7 +893,7 @@ struct PairCfg {
 
 constexpr int kThreadsPair = 352;  // warp 0 TMA, 1 MMA, 2..9 epilogue, 10 scale copies
 
-// SK: the stream-K tail (p.sk_part / p.sk_flag set); a separate instantiation keeps the
+// SK: the stream-K tail (p.sk_part / p.sk_flag / p.sk_ticket set); a separate instantiation keeps the
 // whole-tile kernel's code exactly as without it
 template <int STAGES, bool SK>
 __global__ void __launch_bounds__(kThreadsPair, 1)
@@ -950,12 +952,12 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   // that run at the same time work on neighbouring tiles, which share operands in L2); the
   // k-block iterations of the remaining tiles are cut into one contiguous range per pair,
   // [I * pair / P, I * (pair + 1) / P). Such a range starts inside a tile and may end inside one:
-  // its segments are (tile, k-blocks [kb_lo, kb_hi)). The pair whose segment starts a tile
-  // (kb_lo == 0) finishes it, adding the partial sums of the later pairs that hold the rest of its
-  // k-blocks, in k order (deterministic); those write theirs to the workspace first thing.
+  // its segments are (tile, k-blocks [kb_lo, kb_hi)). Of the pairs that share a tile, the last to
+  // finish its MMAs adds the others' partial sums (from the workspace) to its own, in k order
+  // (deterministic), and writes the outputs.
   const int pair = static_cast<int>(blockIdx.x >> 1), n_pairs = tile_step;
   // the split tail is the last wave of whole tiles plus the remainder, so that every pair's range
-  // covers at least one tile's worth of k-blocks and few pairs share a tile
+  // covers at least one tile's worth of k-blocks and at most two pairs share a tile
   const int full_waves = sk && total / n_pairs > 0 ? total / n_pairs - 1 : 0;
   const int tail0 = full_waves * n_pairs;  // first tile of the split tail
   const int64_t iters = static_cast<int64_t>(total - tail0) * nk;
@@ -1173,64 +1175,112 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       const int64_t row0 = m0 + BM * rank;
       const int64_t row = row0 + 32 * q + lane;
       const int64_t col0 = static_cast<int64_t>(g) * p.n_feat + n0 + 128 * half;
-      // Partial slots are [pair][rank][8 warps][32 x 16-byte column groups][32 lanes]: a warp's
-      // 16 KB are contiguous and each of its 16-byte stores or loads covers 512 contiguous bytes.
-      // Rows past the last token hold zeros on both sides and are neither stored nor loaded.
+      // A warp's share of a split tile is 32 rows x 128 columns. Partial slots are [pair][split
+      // segment 0/1][rank][8 warps][32 x 16-byte column groups][32 lanes]: a warp's 16 KB are
+      // contiguous and each of its 16-byte stores or loads covers 512 contiguous bytes. Rows past
+      // the last token hold zeros on every side and are neither stored nor loaded.
       const bool live = row < p.T;
-      auto slot_of = [&](int pr) {
-        return p.sk_part + (static_cast<int64_t>(pr * 2 + static_cast<int>(rank)) * 8 + ew) * (32 * 32) + lane;
-      };
-      if (sk && kb_lo == 0 && kb_hi < nk && row0 < p.z_mp128) {
-        // This segment starts a tile of the split tail (always the pair's last segment, so the
-        // accumulator may stay in TMEM): take each later pair's partial as its flag rises, 16
-        // columns' loads in flight per contributor, and add it in k order, chunk by chunk.
-        const int64_t end = (static_cast<int64_t>(t - tail0) + 1) * nk;
-        int p_end = pair + 1;  // the contributors are the pairs pair + 1 .. p_end - 1
-        while (p_end < n_pairs && range_lo(p_end) < end) ++p_end;
-        bool ok = true;
-        for (int p2 = pair + 1; p2 < p_end && ok; ++p2) {
-          if (range_lo(p2 + 1) == range_lo(p2)) continue;  // an empty range holds nothing
-          if (lane == 0) ok = wait_flag_gpu(p.sk_flag + (p2 * 2 + static_cast<int>(rank)) * 8 + ew);
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        }
-        if (!ok) {
-          if (lane == 0) {
-            *abort_flag = 1;
-            report_timeout(p.status);
+      if (sk && (kb_lo > 0 || kb_hi < nk) && row0 < p.z_mp128) {
+        // A tile of the split tail shared with other pairs: its k-blocks lie in the consecutive
+        // ranges of pairs [q_lo, q_hi). Every sharer takes a ticket once its MMAs are done; the
+        // last to arrive finishes the tile, the others store their partial sums and raise their
+        // flag. So nobody waits for a pair that has not started: the finisher waits only for
+        // sharers that already hold a ticket and are storing.
+        const int tt = t - tail0;
+        const int64_t k_lo = static_cast<int64_t>(tt) * nk, k_hi = k_lo + nk;
+        int q_lo = pair, q_hi = pair + 1;
+        while (q_lo > 0 && range_lo(q_lo) > k_lo) --q_lo;
+        while (q_hi < n_pairs && range_lo(q_hi) < k_hi) ++q_hi;
+        // a pair's split segments: 0 = the first of its range, 1 = the last
+        auto unit = [&](int qq) {
+          const int j = range_lo(qq) / nk == tt ? 0 : 1;
+          return ((qq * 2 + j) * 2 + static_cast<int>(rank)) * 8 + ew;
+        };
+        auto slot = [&](int qq) { return p.sk_part + static_cast<int64_t>(unit(qq)) * (32 * 32) + lane; };
+        int sharers = 0;
+        for (int qq = q_lo; qq < q_hi; ++qq) sharers += range_lo(qq + 1) > range_lo(qq) ? 1 : 0;
+        int32_t* ticket = p.sk_ticket + (tt * 2 + static_cast<int>(rank)) * 8 + ew;
+        int arrived = 0;
+        if (lane == 0) arrived = atomicAdd(ticket, 1);
+        arrived = __shfl_sync(0xffffffffu, arrived, 0);
+        if (arrived == sharers - 1) {
+          bool ok = true;
+          for (int qq = q_lo; qq < q_hi && ok; ++qq) {
+            if (qq == pair || range_lo(qq + 1) == range_lo(qq)) continue;
+            if (lane == 0) ok = wait_flag_gpu(p.sk_flag + unit(qq));
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           }
-          break;
-        }
-        uint32_t word = 0;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t a[32];
-          tmem_ld_x32(t_lane + 32 * c, a);
-          tmem_ld_wait();
-          for (int p2 = pair + 1; p2 < p_end && live; ++p2) {
-            if (range_lo(p2 + 1) == range_lo(p2)) continue;
-            const float4* src = slot_of(p2) + c * 8 * 32;
-            float4 u[8];
-#pragma unroll
-            for (int v = 0; v < 8; ++v) u[v] = __ldcg(src + v * 32);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              a[4 * v] = __float_as_uint(__uint_as_float(a[4 * v]) + u[v].x);
-              a[4 * v + 1] = __float_as_uint(__uint_as_float(a[4 * v + 1]) + u[v].y);
-              a[4 * v + 2] = __float_as_uint(__uint_as_float(a[4 * v + 2]) + u[v].z);
-              a[4 * v + 3] = __float_as_uint(__uint_as_float(a[4 * v + 3]) + u[v].w);
+          if (!ok) {
+            if (lane == 0) {
+              *abort_flag = 1;
+              report_timeout(p.status);
             }
+            break;
           }
-          epi_row_chunk(p, a, row, col0 + 32 * c, word, c);
+          // per 32-column chunk: this pair's own sums stay in TMEM until read here; the other
+          // sharer's come from its slot, 8 loads in flight. At most two pairs share a tile (every
+          // range spans at least one tile's k-blocks), and the sum of two fp32 terms does not
+          // depend on their order, so the bytes are the same whichever of the two finishes.
+          uint32_t word = 0;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t a[32];
+            tmem_ld_x32(t_lane + 32 * c, a);
+            tmem_ld_wait();
+            for (int qq = q_lo; qq < q_hi && live; ++qq) {
+              if (qq == pair || range_lo(qq + 1) == range_lo(qq)) continue;
+              const float4* src = slot(qq) + c * 8 * 32;
+              float4 u[8];
+#pragma unroll
+              for (int x = 0; x < 8; ++x) u[x] = __ldcg(src + x * 32);
+#pragma unroll
+              for (int x = 0; x < 8; ++x) {
+                a[4 * x] = __float_as_uint(__uint_as_float(a[4 * x]) + u[x].x);
+                a[4 * x + 1] = __float_as_uint(__uint_as_float(a[4 * x + 1]) + u[x].y);
+                a[4 * x + 2] = __float_as_uint(__uint_as_float(a[4 * x + 2]) + u[x].z);
+                a[4 * x + 3] = __float_as_uint(__uint_as_float(a[4 * x + 3]) + u[x].w);
+              }
+            }
+            epi_row_chunk(p, a, row, col0 + 32 * c, word, c);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            for (int qq = q_lo; qq < q_hi; ++qq)
+              if (qq != pair && range_lo(qq + 1) > range_lo(qq)) p.sk_flag[unit(qq)] = 0;
+            *ticket = 0;  // every sharer has taken its ticket: ready for the next launch
+            if (leader)
+              mbar_arrive(bar_acce);
+            else
+              mbar_arrive_remote(acce0);
+          }
+          continue;
         }
+        uint32_t acc[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld_x32(t_lane + 32 * c, acc[c]);
+        tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          for (int p2 = pair + 1; p2 < p_end; ++p2) p.sk_flag[(p2 * 2 + static_cast<int>(rank)) * 8 + ew] = 0;
           if (leader)
             mbar_arrive(bar_acce);
           else
             mbar_arrive_remote(acce0);
         }
+        if (live) {
+          float4* dst = slot(pair);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+              __stcg(dst + (c * 8 + x) * 32,
+                     make_float4(__uint_as_float(acc[c][4 * x]), __uint_as_float(acc[c][4 * x + 1]),
+                                 __uint_as_float(acc[c][4 * x + 2]), __uint_as_float(acc[c][4 * x + 3])));
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(p.sk_flag + unit(pair), 1);
         continue;
       }
       uint32_t acc[4][32];
@@ -1246,24 +1296,6 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           mbar_arrive_remote(acce0);
       }
       if (row0 >= p.z_mp128) continue;  // this half of a ragged last pair tile holds no token
-      if (sk && kb_lo > 0) {
-        // a later part of a tile's k-blocks: this warp's 32 rows x 128 columns of fp32 partial
-        // sums go to the pair's slot, then its flag rises for the pair that finishes the tile
-        if (live) {
-          float4* dst = slot_of(pair);
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              __stcg(dst + (c * 8 + v) * 32,
-                     make_float4(__uint_as_float(acc[c][4 * v]), __uint_as_float(acc[c][4 * v + 1]),
-                                 __uint_as_float(acc[c][4 * v + 2]), __uint_as_float(acc[c][4 * v + 3])));
-        }
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) st_release_gpu(p.sk_flag + (pair * 2 + static_cast<int>(rank)) * 8 + ew, 1);
-        continue;
-      }
       uint32_t word = 0;
 #pragma unroll
       for (int c = 0; c < 4; ++c) epi_row_chunk(p, acc[c], row, col0 + 32 * c, word, c);
@@ -1463,7 +1495,9 @@ cudaError_t launch_swap(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   const int slots = num_sms() * ctas_per_sm<BN, STAGES, ACT>();
   const int s = pick_splits<BN, STAGES, ACT>(tiles, kb_total, slots);
   // The one-CTA-per-SM band (128-token tiles, 6 stages): when the power-of-two split leaves SMs
-  // idle (wo_b at T <= 128: 40 tiles x 2 ranks on 152 SMs), 3 ranks fill more of them (120 CTAs).
+  // idle and 3 ranks of every tile still fit in one wave, K is cut over 3 ranks. The gate is on
+  // the tile and SM counts, not on the operand: at the DeepSeek-V4.1 shapes wo_b (40 tiles: 80
+  // CTAs -> 120) takes it, while wo_a (64 tiles: 3 ranks would need 192 CTAs) stays on two.
   if constexpr (BN == 128 && STAGES == 6 && ACT == kActMx) {
     constexpr int US = 3;
     constexpr bool fits = BN * 512 + 2048 * ((BN / 4 + US - 1) / US) * (US - 1) <= Cfg<BN, STAGES, ACT>::OFF_SF;
@@ -1495,8 +1529,12 @@ cudaError_t launch_normal(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
 
 }  // namespace
 
-constexpr int64_t kSkSlotBytes = 2 * 128 * 256 * 4;  // one pair: two CTAs' 128 x 256 fp32 partials
-constexpr int64_t kSkFlagBytes = 2 * 8 * 4;          // one pair: two CTAs x 8 epilogue warps
+// Split workspace per SM pair: partial sums of two segments (the first and last of a pair's
+// range) for both CTAs, 128 x 256 fp32 each; their ready flags (2 segments x 2 CTAs x 8 epilogue
+// warps); and the arrival tickets of two tail tiles (the tail holds fewer than 2 tiles per pair).
+constexpr int64_t kSkSlotBytes = 2 * 2 * 128 * 256 * 4;
+constexpr int64_t kSkFlagBytes = 2 * 2 * 8 * 4;
+constexpr int64_t kSkTicketBytes = 2 * 2 * 8 * 4;
 
 // Clusters of the pair kernel that fit on the device at once (1 CTA per SM by its shared memory).
 template <int STAGES>
@@ -1544,10 +1582,11 @@ cudaError_t launch_pair(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   int pairs = static_cast<int>(want < max_pairs ? want : max_pairs);
   // Stream-K when a workspace is given and whole tiles would leave a ragged last wave that costs
   // more than the split's fixed cost: every pair that can be resident at once then takes an
-  // equal share of the tail's k-block iterations (all of them must be resident together, since a
-  // pair that starts a tile waits for the partials of the pairs after it). Whole tiles take
-  // floor(tiles / P) waves plus half a tile (the last wave split in two halves) or a whole one;
-  // measured: wo_b (64 k-blocks) gains at 1024..4096 tokens, wo_a (32 k-blocks) never does.
+  // equal share of the tail's k-block iterations. (Residency is a matter of speed only: a pair
+  // never waits for one that has not started, so the launch completes with any number of SMs
+  // available.) Whole tiles take floor(tiles / P) waves plus half a tile (the last wave split in
+  // two halves) or a whole one; measured: wo_b (64 k-blocks) gains at 1024..4096 tokens, wo_a
+  // (32 k-blocks) never does.
   if (l.workspace != nullptr && tiles % max_pairs != 0) {
     const int resident = pair_clusters_resident<STAGES>();
     const int sk_pairs = resident < max_pairs ? resident : max_pairs;
@@ -1561,6 +1600,7 @@ cudaError_t launch_pair(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
       uint8_t* ws = static_cast<uint8_t*>(l.workspace);
       ka.sk_part = reinterpret_cast<float4*>(ws);
       ka.sk_flag = reinterpret_cast<int32_t*>(ws + static_cast<int64_t>(max_pairs) * kSkSlotBytes);
+      ka.sk_ticket = reinterpret_cast<int32_t*>(ws + static_cast<int64_t>(max_pairs) * (kSkSlotBytes + kSkFlagBytes));
       pairs = sk_pairs;
       kern = kern_sk;
     }
@@ -1592,7 +1632,9 @@ cudaError_t launch_pair(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, kern, tma_act, tma_wt, tma_wt64, tma_sfa, tma_sfb, ka);
 }
 
-int64_t split_workspace_bytes() { return static_cast<int64_t>(num_sms() / 2) * (kSkSlotBytes + kSkFlagBytes); }
+int64_t split_workspace_bytes() {
+  return static_cast<int64_t>(num_sms() / 2) * (kSkSlotBytes + kSkFlagBytes + kSkTicketBytes);
+}
 
 cudaError_t launch_gemm(const GemmLaunch& l, cudaStream_t stream) {
   KArgs ka = {};

@@ -27,19 +27,19 @@ def test_every_declared_symbol_is_exported(lib):
     from mxfp8_activation_quant_gb300 import _lib
 
     names = declared_functions()
-    assert len(names) == 15, names
+    assert len(names) == 16, names
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(_lib.SIGNATURES)
 
 
 def test_version_and_status_strings(lib):
-    assert lib.mxq_abi_version() == 2
+    assert lib.mxq_abi_version() == 3
     for code, name in [(0, b"MXQ_OK"), (2, b"MXQ_ERR_UNSUPPORTED_SHAPE"), (6, b"MXQ_ERR_TIMEOUT")]:
         assert lib.mxq_status_string(code) == name
     assert lib.mxq_status_bytes() >= 4
-    # two 128 KB partial slots and 64 bytes of flags per SM pair
-    assert lib.mxq_workspace_bytes() > 0 and lib.mxq_workspace_bytes() % (2 * 128 * 1024 + 64) == 0
+    # four 128 KB partial slots, 128 bytes of flags and 128 bytes of tickets per SM pair
+    assert lib.mxq_workspace_bytes() > 0 and lib.mxq_workspace_bytes() % (4 * 128 * 1024 + 256) == 0
 
 
 def test_sf_bytes_match_oracle_layout_sizes(lib, oracle):

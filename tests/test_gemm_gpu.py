@@ -12,6 +12,7 @@ Token counts follow the pages' tests: 1, 129, 8193 tokens and M in {1, 4, 7, 64,
 decode and prefill sweeps."""
 import ctypes
 import re
+import time
 
 import numpy as np
 import pytest
@@ -76,11 +77,19 @@ def test_gemm_exact_integers(mxq, oracle, T, N, K):
 # ------------------------------------------------------------------------------------------
 # stream-K split of the CTA-pair GEMM (T > 384 with a workspace)
 # ------------------------------------------------------------------------------------------
+SK_SLOTS_PER_PAIR = 4 * 128 * 1024  # partial sums: two segments x two CTAs, 128 x 256 fp32
+SK_PER_PAIR = SK_SLOTS_PER_PAIR + 256  # + 128 bytes of ready flags and 128 of tickets
+
+
 def _flags_zero(mxq, ws):
-    """The flag bytes (after one 256 KB partial slot pair per SM pair) are all zero."""
-    per_pair = 2 * 128 * 1024 + 64
-    pairs = ws.numel() // per_pair
-    return bool((ws[pairs * 2 * 128 * 1024:] == 0).all())
+    """The flag and ticket bytes (after the partial slots of every SM pair) are all zero."""
+    pairs = ws.numel() // SK_PER_PAIR
+    return bool((ws[pairs * SK_SLOTS_PER_PAIR:] == 0).all())
+
+
+def _slots_written(ws):
+    pairs = ws.numel() // SK_PER_PAIR
+    return bool((ws[: pairs * SK_SLOTS_PER_PAIR] != 0).any())
 
 
 @pytest.mark.parametrize("T,N,K", [(1000, 5120, 8192), (2000, 5120, 8192)])
@@ -101,12 +110,43 @@ def test_split_k_exact_integers(mxq, oracle, T, N, K):
     mxq.gemm_mxfp8_bf16(A, B, whole, workspace=False)
     torch.cuda.synchronize()
     assert out.intact() and _flags_zero(mxq, ws)
-    pairs = ws.numel() // (2 * 128 * 1024 + 64)
-    assert bool((ws[: pairs * 2 * 128 * 1024] != 0).any())  # partial slots were written: the split ran
+    assert _slots_written(ws)  # partial slots were written: the split ran
     got = u8(out.body).view(np.uint16).reshape(T, N)
     want = oracle.bf16_round(a.double().numpy() @ b.double().numpy().T)
     assert np.array_equal(got, want)
     assert np.array_equal(got, bf16_bits(whole))
+
+
+def test_split_k_completes_while_other_work_holds_sms(mxq, oracle):
+    """No pair of the split tail waits for one that has not started: with all but 16 SM pairs held
+    by another stream's kernel for 1.5 s (longer than the pipelines' 1 s bounded waits), the split
+    GEMM (76 pairs at T = 2000) still completes while that kernel holds its SMs, with MXQ_OK, the
+    exact product and the flags and tickets back at zero."""
+    T, N, K = 2000, 5120, 8192
+    rng = np.random.default_rng(29)
+    a = int_matrix(rng, T, K)
+    b = int_matrix(rng, N, K)
+    A, B = gpu_mx(mxq, a), gpu_mx(mxq, b)
+    ws = torch.zeros(mxq.workspace_bytes(), dtype=torch.uint8, device="cuda")
+    out = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    st = mxq.new_status()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    s_hold, s_gemm = torch.cuda.Stream(), torch.cuda.Stream()
+    e_hold, e_gemm = torch.cuda.Event(), torch.cuda.Event()
+    torch.cuda.synchronize()
+    mxq.selftest_hold_sms(sms // 2 - 16, 1_500_000, stream=s_hold)
+    e_hold.record(s_hold)
+    time.sleep(0.05)  # the holding kernel takes its SMs first
+    mxq.gemm_mxfp8_bf16(A, B, out, status=st, stream=s_gemm, workspace=ws)
+    e_gemm.record(s_gemm)
+    e_gemm.synchronize()
+    held_still = not e_hold.query()
+    torch.cuda.synchronize()
+    mxq.check_status(st)
+    assert held_still, "the GEMM did not run beside the holding kernel"
+    assert _flags_zero(mxq, ws) and _slots_written(ws)
+    want = oracle.bf16_round(a.double().numpy() @ b.double().numpy().T)
+    assert np.array_equal(bf16_bits(out), want)
 
 
 def test_split_k_grouped_fused_epilogue(mxq, oracle):
@@ -130,8 +170,7 @@ def test_split_k_grouped_fused_epilogue(mxq, oracle):
         outs.append((zq, ztl, zb))
     torch.cuda.synchronize()
     assert _flags_zero(mxq, ws)
-    pairs = ws.numel() // (2 * 128 * 1024 + 64)
-    assert bool((ws[: pairs * 2 * 128 * 1024] != 0).any())  # the split ran
+    assert _slots_written(ws)  # the split ran
     (zq, ztl, zb), (zq_w, ztl_w, zb_w) = outs
     for gbuf in (zq, ztl, zb, zq_w, ztl_w, zb_w):
         assert gbuf.intact()
@@ -261,12 +300,15 @@ def launched_kernels(fn):
     profiler records no kernels at all in this environment."""
     from torch.profiler import ProfilerActivity, profile
 
-    torch.cuda.synchronize()
-    with profile(activities=[ProfilerActivity.CUDA]) as prof:
-        fn()
+    for _ in range(2):  # a process's first profiling session may come back empty
         torch.cuda.synchronize()
-    names = [e.name for e in prof.events() if "cuda" in str(getattr(e, "device_type", "")).lower()]
-    return names or None
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            fn()
+            torch.cuda.synchronize()
+        names = [e.name for e in prof.events() if "cuda" in str(getattr(e, "device_type", "")).lower()]
+        if names:
+            return names
+    return None
 
 
 @pytest.mark.parametrize("T", [100, 128])
