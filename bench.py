@@ -3,14 +3,18 @@
 One step = one pass of the whole hot path over one batch of T tokens, inputs resident in HBM:
   rmsnorm_dual_out  x [T, 5120] -> y bf16 + y MXFP8 (int32-packed scales)
   mxfp8_quantize    attention output o [T, 8*4096] bf16 -> MXFP8 (F8_128x4 scales)
-  wo_a einsum       o -> z MXFP8 (fused epilogue, F8_128x4 scales)   } the _o_proj pair of
-  wo_b GEMM         z -> out bf16 [T, 5120]                           } o_proj_mxfp8
+  o_proj_mxfp8      the _o_proj pair, one call: wo_a einsum o -> z MXFP8 (fused epilogue,
+                    F8_128x4 scales), then wo_b z -> out bf16 [T, 5120] (a programmatic
+                    dependent launch)
 (DeepSeek-V4.1-Flash TP1 shapes from the vLLM page "[Perf][DSv4.1] MegaAttn: wo_a writes
 wo_b's MXFP8 input", Validation). L2 is flushed before every step (cold L2, as on that page);
-each kernel is timed with CUDA events on the launching stream and the flush is outside the
+each call is timed with CUDA events on the launching stream and the flush is outside the
 events. `value` is tokens/s through the whole chain, summed over ranks (weak scaling: every
-rank runs its own replica). Per-kernel us, GB/s, TFLOP/s and roofline fractions are reported
-alongside. `--impl reference` times the CPU oracle on a bounded sample of the same workload.
+rank runs its own replica). Per-call us, GB/s, TFLOP/s and roofline fractions are reported
+alongside, and a compact `sweep` object times every configuration of the metric the way the
+page does (each call replayed from a CUDA graph, L2 flushed before it): the _o_proj pair fused
+and unfused over T = 1..32768, the quantizer and RMSNorm at two sizes each. `--impl reference`
+times the CPU oracle on a bounded sample of the same workload.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--tokens T] [--impl reference] [--sweep]
 """
@@ -36,6 +40,8 @@ G, NA, KA, NB, H = 8, 1024, 4096, 5120, 5120
 KB = G * NA
 FLOP_PER_TOKEN = 2 * G * NA * KA + 2 * NB * KB
 WEIGHT_BYTES = G * NA * KA + NB * KB + (G * NA * KA + NB * KB) // 32
+NOMINAL_HBM_GBS = 8000.0         # GB300 HBM3e, nominal
+NOMINAL_MXFP8_TFLOPS = 4500.0    # GB300 dense fp8 tensor rate, nominal
 
 
 def load_peaks():
@@ -96,7 +102,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except Exception:
@@ -211,39 +217,55 @@ def run_gpu(args):
         mxq.mxfp8_quantize(o, oq, None, None, osf)
         if ev is not None:
             ev[2].record(stream)
-        mxq.wo_a_einsum_mxfp8(O, WA, T, G, NA, KA, z_q=zq, z_sf_128x4=zsf, status=status)
+        mxq.o_proj_mxfp8(O, WA, WB, T, G, NA, KA, NB, zq, zsf, out, status=status)
         if ev is not None:
             ev[3].record(stream)
-        mxq.gemm_mxfp8_bf16(Z, WB, out, status=status)
-        if ev is not None:
-            ev[4].record(stream)
 
-    KERNELS_PER_STEP = 4
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    sampler = ClockSampler(dev.index)
-    with sampler:  # clocks sampled from the warm-up through the end of the timed region
-        for i in range(args.warmup):
-            flush.fill_(i & 0xFF)
-            step()
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.fill_((i + 7) & 0xFF)  # cold L2 before every step, outside the events
-            step(evs[i])
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
+    KERNELS_PER_STEP = 4  # rmsnorm_dual_kernel, quantize_kernel, wo_a and wo_b GEMM kernels
+    NPARTS = 3
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(NPARTS + 1)] for _ in range(args.steps)]
+    # clocks are sampled from the warm-up through the timed region and the compact sweep (the
+    # timed steps alone last a few milliseconds, shorter than the sampling period)
+    sampler = ClockSampler(dev.index).__enter__()
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_((i + 7) & 0xFF)  # cold L2 before every step, outside the events
+        step(evs[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
     if world > 1:
         dist.barrier()
     mxq.check_status(status)
 
-    parts = [[evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)] for j in range(4)]
-    step_ms = [sum(parts[j][i] for j in range(4)) for i in range(args.steps)]
+    parts = [[evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)] for j in range(NPARTS)]
+    step_ms = [sum(parts[j][i] for j in range(NPARTS)) for i in range(args.steps)]
     total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
     tokens_per_s = whole_job_rate(world, T, args.steps, total_ms)
+
+    # The two GEMMs as separate launches (no programmatic overlap), each between its own events,
+    # cold L2: how the pair's time divides (reported beside the step, not part of it).
+    sep = [[], []]
+    for i in range(max(3, args.steps // 2) + 3):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        flush.fill_(i & 0xFF)
+        e[0].record(stream)
+        mxq.wo_a_einsum_mxfp8(O, WA, T, G, NA, KA, z_q=zq, z_sf_128x4=zsf, status=status)
+        e[1].record(stream)
+        mxq.gemm_mxfp8_bf16(Z, WB, out, status=status)
+        e[2].record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            sep[0].append(e[0].elapsed_time(e[1]))
+            sep[1].append(e[1].elapsed_time(e[2]))
+    mxq.check_status(status)
 
     # end-to-end through the public API: pinned host inputs -> device -> chain -> host result.
     # Two buffer slots and three streams: step i+1's inputs go in (copy stream) while step i
@@ -302,35 +324,49 @@ def run_gpu(args):
 
     hbm, bf16_tf, peak_kind = load_peaks()
     mx_tf = 2.0 * bf16_tf  # fp8 dense rate = 2x bf16 (nominal 4.5 / 2.25 PFLOP/s)
-    names = ["rmsnorm_dual_out", "mxfp8_quantize", "wo_a_fused_mxfp8", "wo_b_mxfp8"]
-    byts = [rms_bytes(T), quant_bytes(T, G * KA), wo_a_bytes(T), wo_b_bytes(T)]
-    flops = [0, 0, wo_a_flops(T), wo_b_flops(T)]
-    detail = {}
-    for j, n in enumerate(names):
-        us = 1e3 * statistics.mean(parts[j])
-        d = {"us": round(us, 3), "GB/s": round(byts[j] / us / 1e3, 1)}
-        roof_us = max(byts[j] / hbm / 1e3, flops[j] / mx_tf / 1e6) if flops[j] else byts[j] / hbm / 1e3
-        if flops[j]:
-            d["TFLOP/s"] = round(flops[j] / us / 1e6, 1)
+
+    def rate(byts, flops, us):
+        d = {"us": round(us, 3), "GB/s": round(byts / us / 1e3, 1)}
+        roof_us = max(byts / hbm / 1e3, flops / mx_tf / 1e6)
+        if flops:
+            d["TFLOP/s"] = round(flops / us / 1e6, 1)
         d["roofline_us"] = round(roof_us, 3)
         d["frac"] = round(roof_us / us, 4)
-        detail[n] = d
-    o_proj_us = detail["wo_a_fused_mxfp8"]["us"] + detail["wo_b_mxfp8"]["us"]
-    detail["o_proj"] = {"us_per_call": round(o_proj_us, 3),
-                        "TFLOP/s": round(FLOP_PER_TOKEN * T / o_proj_us / 1e6, 1)}
-    dom = max(range(4), key=lambda j: statistics.mean(parts[j]))
-    dom_us = 1e3 * statistics.mean(parts[dom])
-    if flops[dom] and flops[dom] / mx_tf / 1e6 >= byts[dom] / hbm / 1e3:
-        roof = {"kernel": names[dom], "bound": "tensor", "achieved": round(flops[dom] / dom_us / 1e6, 1),
-                "peak": round(mx_tf, 1), "unit": "TFLOP/s",
-                "peak_note": f"{peak_kind} bf16 burst x 2 (fp8/bf16 nominal ratio)"}
-    else:
-        roof = {"kernel": names[dom], "bound": "hbm", "achieved": round(byts[dom] / dom_us / 1e3, 1),
-                "peak": hbm, "unit": "GB/s", "peak_note": f"{peak_kind} copy bandwidth"}
-    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = traffic_for(names[dom], T)
+        if flops:
+            d["frac_nominal"] = round(max(byts / NOMINAL_HBM_GBS / 1e3, flops / NOMINAL_MXFP8_TFLOPS / 1e6) / us, 4)
+        return d
 
+    mean_us = [1e3 * statistics.mean(pj) for pj in parts]
+    o_proj_bytes, o_proj_flops = wo_a_bytes(T) + wo_b_bytes(T), FLOP_PER_TOKEN * T
+    detail = {"rmsnorm_dual_out": rate(rms_bytes(T), 0, mean_us[0]),
+              "mxfp8_quantize": rate(quant_bytes(T, G * KA), 0, mean_us[1]),
+              "o_proj_mxfp8": rate(o_proj_bytes, o_proj_flops, mean_us[2]),
+              "wo_a_separate_launch": rate(wo_a_bytes(T), wo_a_flops(T), 1e3 * statistics.mean(sep[0])),
+              "wo_b_separate_launch": rate(wo_b_bytes(T), wo_b_flops(T), 1e3 * statistics.mean(sep[1]))}
+    # the dominant call of the step: the _o_proj pair (its two kernels, one call)
+    dom = max(range(NPARTS), key=lambda j: mean_us[j])
+    dom_name = ["rmsnorm_dual_out", "mxfp8_quantize", "o_proj_mxfp8"][dom]
+    dom_b, dom_f = [(rms_bytes(T), 0), (quant_bytes(T, G * KA), 0), (o_proj_bytes, o_proj_flops)][dom]
+    dom_us = mean_us[dom]
+    if dom_f and dom_f / mx_tf / 1e6 >= dom_b / hbm / 1e3:
+        roof = {"kernel": dom_name + (" (wo_a + wo_b launches of one call)" if dom == 2 else ""),
+                "bound": "tensor", "achieved": round(dom_f / dom_us / 1e6, 1),
+                "peak": round(mx_tf, 1), "unit": "TFLOP/s",
+                "peak_note": f"{peak_kind} bf16 burst x 2 (fp8/bf16 nominal ratio)",
+                "peak_nominal": NOMINAL_MXFP8_TFLOPS}
+        roof["frac_nominal"] = round(roof["achieved"] / NOMINAL_MXFP8_TFLOPS, 4)
+    else:
+        roof = {"kernel": dom_name, "bound": "hbm", "achieved": round(dom_b / dom_us / 1e3, 1),
+                "peak": hbm, "unit": "GB/s", "peak_note": f"{peak_kind} copy bandwidth",
+                "peak_nominal": NOMINAL_HBM_GBS}
+        roof["frac_nominal"] = round(roof["achieved"] / NOMINAL_HBM_GBS, 4)
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = traffic_for(dom_name, T)
+
+    sweep_res = compact_sweep(mxq, synth, torch, dev, WA, WB) if rank == 0 and not args.no_sweep else None
+    sampler.__exit__(None, None, None)
     clocks = sampler.summary()
+    clocks["window"] = "warm-up, timed steps and the compact sweep"
     res = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -345,6 +381,8 @@ def run_gpu(args):
         "clocks": clocks,
         "wall_ms_per_step_incl_l2_flush": round(1e3 * wall / args.steps, 4),
     }
+    if sweep_res is not None:
+        res["sweep"] = sweep_res
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args, T, budget_s=args.cpu_seconds)
     if rank == 0:
@@ -359,9 +397,7 @@ def run_gpu(args):
 # captures (profiles/), keyed by (kernel, tokens), with the sources the capture was taken on and
 # their SHA-1: once those sources change the figure no longer describes the kernel and reads null.
 _GEMM_SRC = ("mxfp8_activation_quant_gb300/csrc/gemm_mxf8.cu", "mxfp8_activation_quant_gb300/csrc/mxq_device.cuh")
-TRAFFIC = {
-    ("wo_b_mxfp8", 4096): (119_257_088 + 38_162_432, _GEMM_SRC, "40b22ced88efc807"),
-}
+TRAFFIC = {}
 
 
 def traffic_for(kernel, T):
@@ -373,22 +409,18 @@ def traffic_for(kernel, T):
     return nbytes if hashlib.sha1(blob).hexdigest()[:16] == sha else None
 
 
-def sweep(args, mxq, synth, torch, dev, WA, WB):
-    """Per-config lines for the sweep tables (not the headline line): quantizer, RMSNorm, and
-    the _o_proj pair fused vs unfused (wo_a bf16 z -> standalone quantize -> wo_b), timed under
-    CUDA-graph replay with a cold L2 (how the pages time the pair: the whole call captured in a
-    CUDA graph, L2 flushed before it)."""
-    hbm, bf16_tf, _ = load_peaks()
-    mx_tf = 2 * bf16_tf
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(4 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
+class GraphTimer:
+    """us per call, the way the pages time _o_proj: the calls replayed from a CUDA graph with an
+    L2 flush before each, minus the same graph holding only the flushes (median of 5 replays)."""
 
-    cap = torch.cuda.Stream(dev)
+    def __init__(self, torch, dev):
+        self.torch = torch
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.flush = torch.empty(max(4 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+        self.cap = torch.cuda.Stream(dev)
 
-    def timeit(fn, reps=20):
-        """us per call, the way the pages time _o_proj: the calls replayed from a CUDA graph with
-        an L2 flush before each, minus the same graph holding only the flushes."""
+    def __call__(self, fn, reps=20):
+        torch, flush, cap = self.torch, self.flush, self.cap
         with torch.cuda.stream(cap):
             fn()
             flush.fill_(0)
@@ -417,72 +449,148 @@ def sweep(args, mxq, synth, torch, dev, WA, WB):
         del g1, g0
         return per[0] - per[1]
 
+
+def o_proj_roofline_us(T, hbm, mx_tf):
+    """max(bytes at the HBM peak, FLOPs at the MXFP8 peak) for the _o_proj pair at T tokens."""
+    byts = WEIGHT_BYTES + T * (G * KA * 33 // 32 + 2 * KB * 33 // 32 + NB * 2)
+    return max(byts / hbm / 1e3, FLOP_PER_TOKEN * T / mx_tf / 1e6)
+
+
+def _o_proj_case(mxq, synth, torch, dev, T):
+    o = synth.o_proj_activation(0, T, device=dev)
+    oq, osf = mxq.quantize(o, layouts=(2,))
+    c = {"o": o, "O": mxq.MXFP8(oq, osf[2]), "oq": oq, "osf": osf[2],
+         "zq": torch.empty((T, KB), dtype=torch.uint8, device=dev), "zsf": mxq.empty_sf(2, T, KB, dev),
+         "zb": torch.empty((T, KB), dtype=torch.bfloat16, device=dev),
+         "out": torch.empty((T, NB), dtype=torch.bfloat16, device=dev)}
+    c["Z"] = mxq.MXFP8(c["zq"], c["zsf"])
+    return c
+
+
+def _o_proj_fused_unfused(mxq, timer, c, T, WA, WB):
+    fused = timer(lambda: mxq.o_proj_mxfp8(c["O"], WA, WB, T, G, NA, KA, NB, c["zq"], c["zsf"], c["out"]))
+
+    def unfused():  # wo_a writes bf16 z, the standalone quantizer, wo_b
+        mxq.wo_a_einsum_mxfp8(c["O"], WA, T, G, NA, KA, z_bf16=c["zb"])
+        mxq.mxfp8_quantize(c["zb"], c["zq"], None, None, c["zsf"])
+        mxq.gemm_mxfp8_bf16(c["Z"], WB, c["out"])
+
+    return fused, timer(unfused)
+
+
+SWEEP_O_PROJ_T = [1, 16, 64, 128, 256, 384, 512, 4096, 32768]
+SWEEP_QUANT_T = [4096, 32768]
+SWEEP_RMS_T = [1024, 4096, 8192]
+
+
+def compact_sweep(mxq, synth, torch, dev, WA, WB):
+    """Every configuration of the metric in one object, timed as the pages time _o_proj (a CUDA
+    graph per call, cold L2): the _o_proj pair fused and unfused, the quantizer, RMSNorm, and
+    this library's own MXFP8 GEMM on a square 8192^3 problem (a measured dense MXFP8 rate)."""
+    hbm, bf16_tf, kind = load_peaks()
+    mx_tf = 2 * bf16_tf
+    timer = GraphTimer(torch, dev)
+    res = {"timing": "CUDA graph per call, L2 flushed before each (graph of flushes alone subtracted), "
+                     "median of 5 replays of 20 calls",
+           "peaks": {"hbm_GB/s": hbm, "mxfp8_TFLOP/s": mx_tf, "kind": kind + " (mxfp8 = 2 x bf16 burst)",
+                     "nominal_hbm_GB/s": NOMINAL_HBM_GBS, "nominal_mxfp8_TFLOP/s": NOMINAL_MXFP8_TFLOPS}}
+    rows = []
+    for T in SWEEP_O_PROJ_T:
+        c = _o_proj_case(mxq, synth, torch, dev, T)
+        fused, unf = _o_proj_fused_unfused(mxq, timer, c, T, WA, WB)
+        r = {"T": T, "fused_us": round(fused, 2), "unfused_us": round(unf, 2), "saving_us": round(unf - fused, 2),
+             "TFLOP/s": round(FLOP_PER_TOKEN * T / fused / 1e6, 1),
+             "roofline_us": round(o_proj_roofline_us(T, hbm, mx_tf), 2),
+             "frac": round(o_proj_roofline_us(T, hbm, mx_tf) / fused, 4),
+             "frac_nominal": round(o_proj_roofline_us(T, NOMINAL_HBM_GBS, NOMINAL_MXFP8_TFLOPS) / fused, 4)}
+        if T <= 16:  # bf16 o quantized inside wo_a (no quantize launch for o either)
+            r["from_bf16_us"] = round(timer(lambda: mxq.o_proj_mxfp8_from_bf16(
+                c["o"], WA, WB, T, G, NA, KA, NB, c["zq"], c["zsf"], c["out"])), 2)
+        rows.append(r)
+        del c
+    res["o_proj"] = rows
+    q = []
+    for T in SWEEP_QUANT_T:
+        xq = synth.quantizer_input(0, T, device=dev)
+        qq = torch.empty((T, KB), dtype=torch.uint8, device=dev)
+        sf = mxq.empty_sf(2, T, KB, dev)
+        us = timer(lambda: mxq.mxfp8_quantize(xq, qq, None, None, sf))
+        b = quant_bytes(T, KB)
+        q.append({"shape": [T, KB], "us": round(us, 2), "GB/s": round(b / us / 1e3, 1),
+                  "frac_hbm": round(b / us / 1e3 / hbm, 4), "frac_nominal": round(b / us / 1e3 / NOMINAL_HBM_GBS, 4)})
+        del xq, qq, sf
+    res["mxfp8_quantize"] = q
+    rm = []
+    for T in SWEEP_RMS_T:
+        xr = synth.rmsnorm_input(0, T, device=dev)
+        gm = synth.rmsnorm_gamma(0, device=dev)
+        yr = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        yrq = torch.empty((T, H), dtype=torch.uint8, device=dev)
+        sf = mxq.empty_sf(1, T, H, dev)
+        us = timer(lambda: mxq.rmsnorm_dual_out(xr, gm, synth.RMS_EPS, yr, yrq, sf_packed=sf))
+        b = rms_bytes(T)
+        rm.append({"shape": [T, H], "us": round(us, 2), "GB/s": round(b / us / 1e3, 1),
+                   "frac_hbm": round(b / us / 1e3 / hbm, 4), "frac_nominal": round(b / us / 1e3 / NOMINAL_HBM_GBS, 4)})
+        del xr, yr, yrq, sf
+    res["rmsnorm_dual_out"] = rm
+    n = 8192
+    A = mxq.MXFP8(*_rand_mx(mxq, synth, n, n, synth.TID_SQ_A, dev))
+    B = mxq.MXFP8(*_rand_mx(mxq, synth, n, n, synth.TID_SQ_B, dev))
+    cc = torch.empty((n, n), dtype=torch.bfloat16, device=dev)
+    us = timer(lambda: mxq.gemm_mxfp8_bf16(A, B, cc), reps=5)
+    tf = 2 * n ** 3 / us / 1e6
+    res["mxfp8_gemm_8192^3"] = {"us": round(us, 2), "TFLOP/s": round(tf, 1), "frac": round(tf / mx_tf, 4),
+                                "frac_nominal": round(tf / NOMINAL_MXFP8_TFLOPS, 4)}
+    # every _o_proj fraction once more against this library's own dense MXFP8 rate
+    for r in rows:
+        r["frac_own_gemm_peak"] = round(o_proj_roofline_us(r["T"], hbm, tf) / r["fused_us"], 4)
+    return res
+
+
+def sweep(args, mxq, synth, torch, dev, WA, WB):
+    """Per-config lines for the design tables (more token counts than the compact object):
+    quantizer, RMSNorm, and the _o_proj pair fused vs unfused with each GEMM alone."""
+    hbm, bf16_tf, _ = load_peaks()
+    mx_tf = 2 * bf16_tf
+    timer = GraphTimer(torch, dev)
     for T in [1, 16, 256, 4096, 32768]:
         x = synth.quantizer_input(0, T, device=dev)
         q = torch.empty((T, KB), dtype=torch.uint8, device=dev)
         sf = mxq.empty_sf(2, T, KB, dev)
-        us = timeit(lambda: mxq.mxfp8_quantize(x, q, None, None, sf))
+        us = timer(lambda: mxq.mxfp8_quantize(x, q, None, None, sf))
         b = quant_bytes(T, KB)
         print(json.dumps({"sweep": "mxfp8_quantize", "T": T, "us": round(us, 3), "GB/s": round(b / us / 1e3, 1),
                           "frac_hbm": round(b / us / 1e3 / hbm, 4)}), flush=True)
         del x, q
-    for T in [1, 64, 1024, 8192]:
+    for T in [1, 64, 1024, 4096, 8192]:
         x = synth.rmsnorm_input(0, T, device=dev)
         g = synth.rmsnorm_gamma(0, device=dev)
         y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         yq = torch.empty((T, H), dtype=torch.uint8, device=dev)
         sf = mxq.empty_sf(1, T, H, dev)
-        us = timeit(lambda: mxq.rmsnorm_dual_out(x, g, synth.RMS_EPS, y, yq, sf_packed=sf))
+        us = timer(lambda: mxq.rmsnorm_dual_out(x, g, synth.RMS_EPS, y, yq, sf_packed=sf))
         b = rms_bytes(T)
         print(json.dumps({"sweep": "rmsnorm_dual_out", "T": T, "us": round(us, 3), "GB/s": round(b / us / 1e3, 1),
                           "frac_hbm": round(b / us / 1e3 / hbm, 4)}), flush=True)
     for T in [1, 2, 4, 8, 16, 64, 128, 256, 384, 512, 1024, 2048, 4096, 8192, 16384, 32768]:
-        o = synth.o_proj_activation(0, T, device=dev)
-        oq, osf = mxq.quantize(o, layouts=(2,))
-        del o
-        O = mxq.MXFP8(oq, osf[2])
-        zq = torch.empty((T, KB), dtype=torch.uint8, device=dev)
-        zsf = mxq.empty_sf(2, T, KB, dev)
-        zb = torch.empty((T, KB), dtype=torch.bfloat16, device=dev)
-        out = torch.empty((T, NB), dtype=torch.bfloat16, device=dev)
-        fused = timeit(lambda: mxq.o_proj_mxfp8(O, WA, WB, T, G, NA, KA, NB, zq, zsf, out))
-
-        def unfused():
-            mxq.wo_a_einsum_mxfp8(O, WA, T, G, NA, KA, z_bf16=zb)
-            mxq.mxfp8_quantize(zb, zq, None, None, zsf)
-            mxq.gemm_mxfp8_bf16(mxq.MXFP8(zq, zsf), WB, out)
-
-        unf = timeit(unfused)
+        c = _o_proj_case(mxq, synth, torch, dev, T)
+        fused, unf = _o_proj_fused_unfused(mxq, timer, c, T, WA, WB)
         extra = {}
         if T <= 16:  # bf16 o quantized inside wo_a, against the quantize launch + the fused pair
-            ob = synth.o_proj_activation(0, T, device=dev)
-            extra["from_bf16_us"] = round(timeit(lambda: mxq.o_proj_mxfp8_from_bf16(
-                ob, WA, WB, T, G, NA, KA, NB, zq, zsf, out)), 3)
-            extra["quantize_then_fused_us"] = round(timeit(lambda: (mxq.mxfp8_quantize(ob, oq, None, None, osf[2]),
-                                                                    mxq.o_proj_mxfp8(O, WA, WB, T, G, NA, KA, NB,
-                                                                                     zq, zsf, out))), 3)
-        wa_us = timeit(lambda: mxq.wo_a_einsum_mxfp8(O, WA, T, G, NA, KA, z_q=zq, z_sf_128x4=zsf))
-        wb_us = timeit(lambda: mxq.gemm_mxfp8_bf16(mxq.MXFP8(zq, zsf), WB, out))
-        byts = WEIGHT_BYTES + T * (G * KA * 33 // 32 + 2 * KB * 33 // 32 + NB * 2)
-        roof = max(byts / hbm / 1e3, FLOP_PER_TOKEN * T / mx_tf / 1e6)
+            extra["from_bf16_us"] = round(timer(lambda: mxq.o_proj_mxfp8_from_bf16(
+                c["o"], WA, WB, T, G, NA, KA, NB, c["zq"], c["zsf"], c["out"])), 3)
+            extra["quantize_then_fused_us"] = round(timer(lambda: (
+                mxq.mxfp8_quantize(c["o"], c["oq"], None, None, c["osf"]),
+                mxq.o_proj_mxfp8(c["O"], WA, WB, T, G, NA, KA, NB, c["zq"], c["zsf"], c["out"]))), 3)
+        wa_us = timer(lambda: mxq.wo_a_einsum_mxfp8(c["O"], WA, T, G, NA, KA, z_q=c["zq"], z_sf_128x4=c["zsf"]))
+        wb_us = timer(lambda: mxq.gemm_mxfp8_bf16(c["Z"], WB, c["out"]))
+        roof = o_proj_roofline_us(T, hbm, mx_tf)
         print(json.dumps({"sweep": "o_proj", "T": T, "fused_us": round(fused, 3), "unfused_us": round(unf, 3),
                           "saving_us": round(unf - fused, 3), "wo_a_us": round(wa_us, 3), "wo_b_us": round(wb_us, 3),
                           "TFLOP/s": round(FLOP_PER_TOKEN * T / fused / 1e6, 1), "roofline_us": round(roof, 3),
                           "frac": round(roof / fused, 4),
                           "weight_GB/s": round(WEIGHT_BYTES / fused / 1e3, 1), **extra}), flush=True)
-        del oq, osf, O, zq, zsf, zb, out
-    # The dense MXFP8 rate this library's own GEMM reaches on a square 8192^3 problem (random
-    # E4M3 operands), beside the two peaks the fractions could be taken against: the nominal
-    # dense fp8 figure and 2x the measured bf16 burst (the one the roofline lines use).
-    n = 8192
-    A = mxq.MXFP8(*_rand_mx(mxq, synth, n, n, synth.TID_SQ_A, dev))
-    B = mxq.MXFP8(*_rand_mx(mxq, synth, n, n, synth.TID_SQ_B, dev))
-    c = torch.empty((n, n), dtype=torch.bfloat16, device=dev)
-    us = timeit(lambda: mxq.gemm_mxfp8_bf16(A, B, c), reps=5)
-    tf = 2 * n ** 3 / us / 1e6
-    print(json.dumps({"sweep": "mxfp8_gemm_8192^3", "us": round(us, 2), "TFLOP/s": round(tf, 1),
-                      "frac_of_2x_measured_bf16": round(tf / mx_tf, 4), "frac_of_nominal_4500": round(tf / 4500.0, 4)}),
-          flush=True)
+        del c
 
 
 def _rand_mx(mxq, synth, rows, cols, tid, dev):
@@ -586,7 +694,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--tokens", type=int, default=4096)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="also print the per-config design-table lines")
+    ap.add_argument("--no-sweep", action="store_true", help="leave the compact sweep out of the line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-tokens", type=int, default=4)
