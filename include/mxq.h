@@ -195,10 +195,11 @@ MXQ_API mxq_status wo_a_einsum_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor
  * gemm_mxfp8_bf16 -- the wo_b MXFP8 GEMM ([MegaAttn] Validation: "wo_b 8192 -> 5120"; it
  * consumes the quantized activation as it is):
  *   out[m, n] = RNE_bf16( sum_k deq(a)[m, k] * deq(b)[n, k] )   (fp32 accumulation)
- *   a : [M, K] MXFP8 activations, b : [N, K] MXFP8 weights, both MXQ_SF_TILED_128X4; for
- *       M <= 16 the activation scales may also be MXQ_SF_PACKED_I32_MN ([KeepMXFP8] Pieces: the
- *       DeepGEMM-layout consumer), moved into the tensor cores' layout inside the kernel with a
- *       bit-identical result. Packed scales with M > 16 return MXQ_ERR_UNSUPPORTED_SHAPE.
+ *   a : [M, K] MXFP8 activations, b : [N, K] MXFP8 weights, both MXQ_SF_TILED_128X4; the
+ *       activation scales may also be MXQ_SF_PACKED_I32_MN ([KeepMXFP8] Pieces: the
+ *       DeepGEMM-layout consumer), at any M: each stage's packed words are moved into the tensor
+ *       cores' layout inside the kernel, with the same tiles and splits, so the result is
+ *       bit-identical to the one from F8_128x4 scales.
  *   out_bf16 : [M, N] bf16, row stride ldo elements.
  *   workspace, workspace_bytes : optional split workspace, as in wo_a_einsum_mxfp8.
  * Requires K % 128 == 0, N % 128 == 0, M >= 1.

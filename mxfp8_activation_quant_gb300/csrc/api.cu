@@ -218,12 +218,13 @@ mxq_status gemm_impl(const mxq_mx_tensor* a, const mxq_mx_tensor* b, int64_t M, 
   if (M <= 0 || N <= 0 || K <= 0 || out_bf16 == nullptr) return MXQ_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % 128 != 0 || ldo < N) return MXQ_ERR_UNSUPPORTED_SHAPE;
   if (N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return MXQ_ERR_UNSUPPORTED_SHAPE;
-  // the activation may carry int32-packed MN-major scales at decode sizes (M <= 16)
+  // the activation may carry int32-packed MN-major scales
   const bool a_packed = a != nullptr && a->sf_layout == MXQ_SF_PACKED_I32_MN;
   mxq_status st = MXQ_OK;
   if (a_packed) {
     if (a->data == nullptr || a->sf == nullptr) return MXQ_ERR_INVALID_ARG;
-    if (M > 16 || K % 128 != 0 || a->rows != M || a->cols != K || a->ld < K) return MXQ_ERR_UNSUPPORTED_SHAPE;
+    if (K % 128 != 0 || a->rows != M || a->cols != K || a->ld < K || M >= (int64_t(1) << 31))
+      return MXQ_ERR_UNSUPPORTED_SHAPE;
     if (!al16(a->data) || !al16(a->sf) || (a->ld % 16) != 0) return MXQ_ERR_MISALIGNED;
   } else if ((st = check_operand(a, M, K)) != MXQ_OK) {
     return st;

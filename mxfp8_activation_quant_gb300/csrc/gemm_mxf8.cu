@@ -95,9 +95,9 @@ struct Cfg {
   static constexpr int SF_COLS = 16;  // TMEM columns per stage slot (4 for A + 4 per B atom, padded)
   // kActBf16: the activation tile arrives as bf16 (BN rows of 128 elements, 256-byte rows, no
   // swizzle) in a staging slot, and the epilogue warps quantize it into the B tile and its
-  // scale atom before the MMAs of the stage. kActPackedSf: the B tile arrives as usual and the
-  // BN packed scale words of the stage land in the staging slot, which the epilogue warps
-  // scatter into the atom.
+  // scale atom before the MMAs of the stage. kActPackedSf: the activation tile arrives as usual
+  // and the stage's packed scale words (one per token row of the tile) land in the staging slot,
+  // which the epilogue warps scatter into the activation's F8_128x4 atom.
   static constexpr int BF_BYTES = ACT == kActBf16 ? BN * 256 : ACT == kActPackedSf ? BN * 4 : 0;
   // bytes on the stage's full barrier; the staged activation part has a barrier of its own, so
   // its conversion starts as soon as it lands, under the larger weight load
@@ -133,6 +133,9 @@ struct Cfg {
   static constexpr int MAX_CO = 512 / TMEM_COLS;
   static constexpr int SMEM_FLOOR = SM_SMEM / (MAX_CO + 1) + 1024;
   static constexpr int SMEM_LAUNCH = SMEM_BYTES > SMEM_FLOOR ? SMEM_BYTES : SMEM_FLOOR;
+  // byte offset of the activation's scale atom in a stage's scale slot (the weight atom is first
+  // in swap-AB, second otherwise)
+  static constexpr int ACT_ATOM = 512;
   // Token (swap-AB) or feature tiles of 16..128 columns: the 128 x 256 tile of this kernel,
   // with two B scale atoms, is not used (the CTA-pair kernel covers 256-wide tiles) and its
   // scale and split-K paths are not validated.
@@ -281,8 +284,9 @@ template <int BN, int STAGES, bool SWAP, int ACT = kActMx, int US = 0>
 __global__ void __launch_bounds__(kThreads, 3)
     gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                      const KArgs p) {
-  static_assert(ACT == kActMx || (SWAP && BN == 16), "converted activations: decode tiles only");
-  static_assert(US == 0 || (SWAP && ACT == kActMx && BN >= 32 && US <= BN / 4), "uneven split: wide tiles");
+  static_assert(ACT == kActMx || ACT == kActPackedSf || (SWAP && BN == 16), "bf16 activations: decode tiles only");
+  static_assert(ACT != kActPackedSf || BN <= 128, "packed activation scales: one activation atom per stage");
+  static_assert(US == 0 || (SWAP && ACT != kActBf16 && BN >= 32 && US <= BN / 4), "uneven split: wide tiles");
   constexpr bool CVT = ACT != kActMx;  // a staged activation part converted by the epilogue warps
   using C = Cfg<BN, STAGES, ACT>;
   extern __shared__ uint8_t smem_raw[];
@@ -367,6 +371,13 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
       for (int j = 0; j < C::SFB_ATOMS; ++j)
         bulk_load(sf_dst0 + s * C::SF_BYTES + 512 * (1 + j), b_sf + ((b_rt0 + j) * b_gp4 + b_kc0 + kb) * 512, 512, fb);
+    } else if (ACT == kActPackedSf) {  // normal orientation: the activation is A (128 token rows)
+      tma_load_2d(a_dst0 + s * C::A_BYTES, &tm_a, fb, static_cast<int32_t>(a_xoff + kb * BK), static_cast<int32_t>(a_row0));
+      const uint32_t ab = bar_act + (fb - bar_full);
+      const int64_t rows = p.act_mp4 - a_row0 < BM ? p.act_mp4 - a_row0 : BM;
+      mbar_arrive_expect_tx(ab, static_cast<uint32_t>(rows * 4));
+      bulk_load(sbase + C::OFF_BF + s * C::BF_BYTES, a_sf + ((a_kc0 + kb) * p.act_mp4 + a_row0) * 4,
+                static_cast<uint32_t>(rows * 4), ab);
     } else {
       tma_load_2d(a_dst0 + s * C::A_BYTES, &tm_a, fb, static_cast<int32_t>(a_xoff + kb * BK), static_cast<int32_t>(a_row0));
       bulk_load(sf_dst0 + s * C::SF_BYTES, a_sf + (a_rt * a_gp4 + a_kc0 + kb) * 512, 512, fb);
@@ -500,11 +511,15 @@ __global__ void __launch_bounds__(kThreads, 3)
   const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16);
   if (ACT == kActPackedSf && epi) {
     // During the mainloop the epilogue warps move each stage's packed scale words into the
-    // F8_128x4 atom: token row r's word (its 4 group bytes) goes to bytes r * 16 .. r * 16 + 3.
+    // activation's F8_128x4 atom: token row r's word (its 4 group bytes) goes to the atom's word
+    // (r % 32) * 4 + r / 32 (bytes (r % 32) * 16 + (r / 32) * 4 ..).
     const int t = static_cast<int>(threadIdx.x) - 64;
-    const int rows = static_cast<int>(p.act_mp4 - b_row0 < BN ? p.act_mp4 - b_row0 : BN);
-    for (int i = t; i < STAGES * 128; i += 128)  // everything else in the atoms stays zero
-      reinterpret_cast<uint32_t*>(smem + C::OFF_SF + (i >> 7) * C::SF_BYTES + 512)[i & 127] = 0u;
+    const int64_t row0 = SWAP ? b_row0 : a_row0;
+    const int tile_rows = SWAP ? BN : BM;
+    const int rows = static_cast<int>(p.act_mp4 - row0 < tile_rows ? p.act_mp4 - row0 : tile_rows);
+    const int atom = SWAP ? C::ACT_ATOM : 0;
+    for (int i = t; i < STAGES * 128; i += 128)  // rows past the packed array's stay zero
+      reinterpret_cast<uint32_t*>(smem + C::OFF_SF + (i >> 7) * C::SF_BYTES + atom)[i & 127] = 0u;
     named_barrier(3, 128);
     for (int i = 0; i < nk; ++i) {
       const int s = i % STAGES;
@@ -515,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       }
       if (t < rows) {
         const uint32_t w = reinterpret_cast<const uint32_t*>(smem + C::OFF_BF + s * C::BF_BYTES)[t];
-        reinterpret_cast<uint32_t*>(smem + C::OFF_SF + s * C::SF_BYTES + 512)[t * 4] = w;
+        reinterpret_cast<uint32_t*>(smem + C::OFF_SF + s * C::SF_BYTES + atom)[(t & 31) * 4 + (t >> 5)] = w;
       }
       fence_proxy_async_smem();  // the scale copy reads the atom through the async proxy
       __syncwarp();
@@ -873,17 +888,26 @@ constexpr int kThreadsP = 320;  // the pair kernel's warps 0..9 (warp 10 is adde
 // on both CTAs' barriers. Each CTA drains its half of the accumulator (its 128 token rows x 256
 // columns, in its own TMEM) with four tcgen05.ld and releases it at once.
 // ------------------------------------------------------------------------------------------
-template <int STAGES>
+// PK: the activation (A) scales arrive int32-packed MN-major: each stage's 128 words of this
+// CTA's token rows land in a staging slot on a barrier of the CTA's own, and warp 10 of each CTA
+// scatters them into the A atom before the even CTA copies the atoms into TMEM.
+template <int STAGES, bool PK = false>
 struct PairCfg {
   static constexpr int A_BYTES = BM * BK;   // this CTA's 128 token rows
   static constexpr int B_BYTES = 128 * BK;  // this CTA's 128 of the 256 weight rows
   static constexpr int SF_BYTES = 512 * 3;  // scale atoms: A (own rows), B (both 128-row atoms)
   // bytes of one stage of both CTAs (counted on the even CTA's barrier) for a tile of n features
-  __host__ __device__ static constexpr uint32_t tx_bytes(int n) { return 2u * (A_BYTES + (n / 2) * BK + 512 + (n / 128) * 512); }
+  // (with PK the A atoms are not among them: the packed words complete on each CTA's own barrier)
+  __host__ __device__ static constexpr uint32_t tx_bytes(int n) {
+    return 2u * (A_BYTES + (n / 2) * BK + (PK ? 0 : 512) + (n / 128) * 512);
+  }
   static constexpr int OFF_B = STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
-  static constexpr int OFF_BAR = OFF_SF + STAGES * SF_BYTES;
-  static constexpr int OFF_MISC = OFF_BAR + (3 * STAGES + 4) * 8;
+  static constexpr int OFF_PK = OFF_SF + STAGES * SF_BYTES;  // PK: STAGES x 512 B of packed words
+  static constexpr int OFF_BAR = OFF_PK + (PK ? STAGES * 512 : 0);
+  // full, empty, scale atoms in TMEM (STAGES each), accf, acce, drain; PK: packed words landed
+  // (this CTA) and both CTAs' atoms scattered (even CTA), STAGES each
+  static constexpr int OFF_MISC = OFF_BAR + ((PK ? 5 : 3) * STAGES + 4) * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int SF_COLS = 16;
   static constexpr int TMEM_COLS = 512;  // 256 accumulator columns + STAGES x 16 scale columns
@@ -894,13 +918,13 @@ struct PairCfg {
 constexpr int kThreadsPair = 352;  // warp 0 TMA, 1 MMA, 2..9 epilogue, 10 scale copies
 
 // SK: the stream-K tail (p.sk_part / p.sk_flag / p.sk_ticket set); a separate instantiation keeps the
-// whole-tile kernel's code exactly as without it
-template <int STAGES, bool SK>
+// whole-tile kernel's code exactly as without it. PK: int32-packed activation scales (PairCfg).
+template <int STAGES, bool SK, bool PK = false>
 __global__ void __launch_bounds__(kThreadsPair, 1)
     gemm_mxf8_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __grid_constant__ CUtensorMap tm_b64, const __grid_constant__ CUtensorMap tm_sfa,
                    const __grid_constant__ CUtensorMap tm_sfb, const KArgs p) {
-  using C = PairCfg<STAGES>;
+  using C = PairCfg<STAGES, PK>;
   constexpr int BN = 256;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sraw = smem_u32(smem_raw);
@@ -912,10 +936,13 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   const uint32_t bar_acce = bar_accf + 8;            // accumulator empty (16 epilogue warps), even CTA
   const uint32_t bar_drain = bar_accf + 16;          // abort path: all tcgen05 ops completed
   const uint32_t bar_sf = bar_accf + 24;             // STAGES x 8 B: scale atoms of a stage in TMEM
+  const uint32_t bar_pk = bar_sf + STAGES * 8;       // PK: STAGES x 8 B, packed words landed (own)
+  const uint32_t bar_scat = bar_pk + STAGES * 8;     // PK: STAGES x 8 B, both atoms scattered (even CTA)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   int* issued_cnt = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
   int* consumed_cnt = reinterpret_cast<int*>(smem + C::OFF_MISC + 12);
+  int* scattered_cnt = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);  // PK
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0 issues the MMAs
   const bool leader = rank == 0;
@@ -1007,9 +1034,15 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     mbar_init(bar_acce, 16);  // one arrival per epilogue warp of both CTAs
     mbar_init(bar_drain, 2);  // the MMA thread and the scale-copy thread
     for (int s = 0; s < STAGES; ++s) mbar_init(bar_sf + 8 * s, 1);
+    if (PK)
+      for (int s = 0; s < STAGES; ++s) {
+        mbar_init(bar_pk + 8 * s, 1);
+        mbar_init(bar_scat + 8 * s, 2);  // warp 10 of each CTA
+      }
     *abort_flag = 0;
     *issued_cnt = 0;
     *consumed_cnt = 0;
+    *scattered_cnt = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -1038,9 +1071,20 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       const int64_t b_first = static_cast<int64_t>(g) * p.n_feat + n0;
       const int64_t b_row = b_first + (nf / 2) * rank;  // this CTA's nf / 2 weight rows
       const int64_t b_atom = (b_first >> 7) * p.wt_gp4;
+      // PK: this CTA's token rows that exist in the packed array (rows >= Mp have no word)
+      const int64_t pk_rows = PK ? (p.act_mp4 - a_row < 0 ? 0 : (p.act_mp4 - a_row < BM ? p.act_mp4 - a_row : BM)) : 0;
       auto load_act = [&](int s, int kb, uint32_t fb) {
         tma_load_2d_pair(sbase + s * C::A_BYTES, &tm_a, fb, static_cast<int32_t>(a_x + kb * BK), static_cast<int32_t>(a_row));
-        tma_load_2d_pair(sbase + C::OFF_SF + s * C::SF_BYTES, &tm_sfa, fb, 0, static_cast<int32_t>(a_atom + kb));
+        if (!PK) {
+          tma_load_2d_pair(sbase + C::OFF_SF + s * C::SF_BYTES, &tm_sfa, fb, 0, static_cast<int32_t>(a_atom + kb));
+        } else if (pk_rows > 0) {
+          const uint32_t pb = bar_pk + 8 * s;
+          mbar_arrive_expect_tx(pb, static_cast<uint32_t>(pk_rows * 4));
+          bulk_load(sbase + C::OFF_PK + s * 512, p.act_sf + (((a_x >> 7) + kb) * p.act_mp4 + a_row) * 4,
+                    static_cast<uint32_t>(pk_rows * 4), pb);
+        } else {
+          mbar_arrive(bar_pk + 8 * s);  // no token row of this CTA has scales: an all-zero atom
+        }
       };
       auto load_wt = [&](int s, int kb, uint32_t fb) {
         const uint32_t sf = sbase + C::OFF_SF + s * C::SF_BYTES;
@@ -1119,6 +1163,68 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       *consumed_cnt = it;
     }
     pdl_launch_dependents();  // every tile of this pair has been issued
+  } else if (warp == 10 && PK) {
+    // ---------------- packed scale words -> A atom (both CTAs), then scale copies (even CTA) ----
+    // Token row r's word goes to the atom's word (r % 32) * 4 + r / 32: lane l writes the four
+    // words of rows l, l + 32, l + 64, l + 96 as one 16-byte store.
+    const uint32_t scat0 = mapa_shared(bar_scat, 0);
+    int it = 0;
+    bool ok = true;
+    for (int w = 0; ok; ++w) {
+      int t, g, nf, kb_lo, kb_hi;
+      int64_t m0, n0;
+      if (!seg(w, t, g, m0, n0, nf, kb_lo, kb_hi)) break;
+      const int64_t a_row = m0 + BM * rank;
+      const int rows = static_cast<int>(p.act_mp4 - a_row < 0 ? 0 : (p.act_mp4 - a_row < BM ? p.act_mp4 - a_row : BM));
+      const bool full_tile = nf == BN;
+      for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait_bounded(bar_pk + 8 * s, ph)) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            report_timeout(p.status);
+          }
+          ok = false;
+          break;
+        }
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(smem + C::OFF_PK + s * 512);
+        uint32_t wv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) wv[j] = lane + 32 * j < rows ? src[lane + 32 * j] : 0u;
+        st_smem_v4(sbase + C::OFF_SF + s * C::SF_BYTES + lane * 16, wv[0], wv[1], wv[2], wv[3]);
+        fence_proxy_async_smem();  // the scale copy reads the atom through the async proxy
+        __syncwarp();
+        if (lane == 0) {
+          if (leader)
+            mbar_arrive(bar_scat + 8 * s);
+          else
+            mbar_arrive_remote(scat0 + 8 * s);
+        }
+        if (leader && lane == 0) {
+          if (!mbar_wait_bounded(bar_full + 8 * s, ph) || !mbar_wait_bounded(bar_scat + 8 * s, ph)) {
+            *abort_flag = 1;
+            report_timeout(p.status);
+            ok = false;
+          } else {
+            tc_fence_after();
+            const uint32_t sf_src = sbase + C::OFF_SF + s * C::SF_BYTES;
+            const uint32_t sfa_t = tmem + BN + s * C::SF_COLS;
+            tc_cp_sf_atom_pair(sfa_t, sdesc_sf_atom(sf_src));
+            tc_cp_sf_atom_pair(sfa_t + 4, sdesc_sf_atom(sf_src + 512));
+            if (full_tile) tc_cp_sf_atom_pair(sfa_t + 8, sdesc_sf_atom(sf_src + 1024));
+            tc_commit_pair(bar_sf + 8 * s, 0x1);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+    }
+    if (lane == 0) *scattered_cnt = it;
   } else if (warp == 10) {
     // ---------------- scale copies (even CTA) ----------------
     if (leader && lane == 0) {
@@ -1306,6 +1412,13 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // both CTAs have left their loops: issue counts and abort flags are final
+  if (PK && warp == 0 && lane == 0) {
+    // packed words this CTA loaded but warp 10 did not take: let them land before leaving
+    const int peer_abort = ld_dsmem_s32(mapa_shared(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u));
+    if (*abort_flag || peer_abort)
+      for (int i = *scattered_cnt; i < *issued_cnt; ++i)
+        (void)mbar_wait_bounded(bar_pk + 8 * (i % STAGES), (i / STAGES) & 1);
+  }
   if (leader && warp == 0 && lane == 0) {
     const int peer_abort = ld_dsmem_s32(mapa_shared(smem_u32(const_cast<int*>(abort_flag)), 1));
     if (*abort_flag || peer_abort) {
@@ -1460,11 +1573,11 @@ int pick_splits(int tiles, int kb_total, int slots) {
 }
 
 // Clusters of US CTAs of the uneven-split swap-AB kernel that fit on the device at once.
-template <int BN, int STAGES, int US>
+template <int BN, int STAGES, int US, int ACT>
 int uneven_clusters_resident() {
   static const int n = [] {
-    using C = Cfg<BN, STAGES, kActMx>;
-    auto kern = gemm_mxf8_kernel<BN, STAGES, true, kActMx, US>;
+    using C = Cfg<BN, STAGES, ACT>;
+    auto kern = gemm_mxf8_kernel<BN, STAGES, true, ACT, US>;
     if (set_smem_attrs(kern, C::SMEM_LAUNCH) != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, static_cast<unsigned>(8 * US));
@@ -1498,11 +1611,11 @@ cudaError_t launch_swap(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   // idle and 3 ranks of every tile still fit in one wave, K is cut over 3 ranks. The gate is on
   // the tile and SM counts, not on the operand: at the DeepSeek-V4.1 shapes wo_b (40 tiles: 80
   // CTAs -> 120) takes it, while wo_a (64 tiles: 3 ranks would need 192 CTAs) stays on two.
-  if constexpr (BN == 128 && STAGES == 6 && ACT == kActMx) {
+  if constexpr (BN == 128 && STAGES == 6 && ACT != kActBf16) {
     constexpr int US = 3;
     constexpr bool fits = BN * 512 + 2048 * ((BN / 4 + US - 1) / US) * (US - 1) <= Cfg<BN, STAGES, ACT>::OFF_SF;
     if (fits && s < US && tiles * s < num_sms() && tiles * US <= slots && kb_total >= 2 * US &&
-        tiles <= uneven_clusters_resident<BN, STAGES, US>()) {
+        tiles <= uneven_clusters_resident<BN, STAGES, US, ACT>()) {
       ka.splits = US;
       ka.kb_per_cta = kb_total;  // all k-blocks: the kernel cuts the uneven ranges
       ka.per_rank_shift = 0;
@@ -1518,13 +1631,13 @@ cudaError_t launch_swap(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   return launch_cfg<BN, STAGES, true, ACT>(l, ka, grid, s, stream);
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int ACT = kActMx>
 cudaError_t launch_normal(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   ka.splits = 1;
   ka.kb_per_cta = l.k_len / BK;
   dim3 grid(static_cast<unsigned>(l.n_feat / BN), static_cast<unsigned>(ceil_div(l.T, BM)),
             static_cast<unsigned>(l.G));
-  return launch_cfg<BN, STAGES, false>(l, ka, grid, 1, stream);
+  return launch_cfg<BN, STAGES, false, ACT>(l, ka, grid, 1, stream);
 }
 
 }  // namespace
@@ -1537,10 +1650,10 @@ constexpr int64_t kSkFlagBytes = 2 * 2 * 8 * 4;
 constexpr int64_t kSkTicketBytes = 2 * 2 * 8 * 4;
 
 // Clusters of the pair kernel that fit on the device at once (1 CTA per SM by its shared memory).
-template <int STAGES>
+template <int STAGES, bool PK>
 int pair_clusters_resident() {
   static const int n = [] {
-    using C = PairCfg<STAGES>;
+    using C = PairCfg<STAGES, PK>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(num_sms()), 1, 1);
     cfg.blockDim = dim3(kThreadsPair, 1, 1);
@@ -1553,7 +1666,7 @@ int pair_clusters_resident() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_mxf8_pair<STAGES, true>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_mxf8_pair<STAGES, true, PK>, &cfg) != cudaSuccess) {
       (void)cudaGetLastError();
       return 0;
     }
@@ -1563,11 +1676,11 @@ int pair_clusters_resident() {
 }
 
 // CTA-pair persistent launch: clusters of two, one CTA per SM, pair tiles of 256 x 256
-template <int STAGES>
+template <int STAGES, bool PK = false>
 cudaError_t launch_pair(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
-  using C = PairCfg<STAGES>;
-  auto kern = gemm_mxf8_pair<STAGES, false>;
-  auto kern_sk = gemm_mxf8_pair<STAGES, true>;
+  using C = PairCfg<STAGES, PK>;
+  auto kern = gemm_mxf8_pair<STAGES, false, PK>;
+  auto kern_sk = gemm_mxf8_pair<STAGES, true, PK>;
   static const cudaError_t attr_err = set_smem_attrs(kern, C::SMEM_BYTES);
   if (attr_err != cudaSuccess) return attr_err;
   static const cudaError_t attr_err_sk = set_smem_attrs(kern_sk, C::SMEM_BYTES);
@@ -1588,7 +1701,7 @@ cudaError_t launch_pair(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   // two halves) or a whole one; measured: wo_b (64 k-blocks) gains at 1024..4096 tokens, wo_a
   // (32 k-blocks) never does.
   if (l.workspace != nullptr && tiles % max_pairs != 0) {
-    const int resident = pair_clusters_resident<STAGES>();
+    const int resident = pair_clusters_resident<STAGES, PK>();
     const int sk_pairs = resident < max_pairs ? resident : max_pairs;
     const int64_t rem = sk_pairs > 0 ? tiles % sk_pairs : 0;
     const double rr_tail = rem == 0 ? 0.0 : (2 * rem <= sk_pairs ? 0.5 : 1.0);
@@ -1609,7 +1722,8 @@ cudaError_t launch_pair(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   if (!make_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, BM)) return cudaErrorInvalidValue;
   if (!make_map(&tma_wt, l.wt, static_cast<int64_t>(l.G) * l.n_feat, l.k_len, l.wt_ld, 128)) return cudaErrorInvalidValue;
   if (!make_map(&tma_wt64, l.wt, static_cast<int64_t>(l.G) * l.n_feat, l.k_len, l.wt_ld, 64)) return cudaErrorInvalidValue;
-  if (!make_sf_map(&tma_sfa, l.act_sf, ceil_div(l.T, 128) * ka.act_gp4)) return cudaErrorInvalidValue;
+  // (with packed activation scales the A atoms are not loaded through this map)
+  if (!make_sf_map(&tma_sfa, PK ? l.wt_sf : l.act_sf, PK ? 1 : ceil_div(l.T, 128) * ka.act_gp4)) return cudaErrorInvalidValue;
   if (!make_sf_map(&tma_sfb, l.wt_sf, ceil_div(static_cast<int64_t>(l.G) * l.n_feat, 128) * ka.wt_gp4))
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
@@ -1676,9 +1790,15 @@ cudaError_t launch_gemm(const GemmLaunch& l, cudaStream_t stream) {
     return launch_swap<16, 3, kActBf16>(l, ka, stream);
   }
   if (l.act_sf_packed) {  // int32-packed activation scales, moved into atoms in the kernel
-    if (l.T > 16) return cudaErrorInvalidValue;
-    return l.has_dependent ? launch_swap<16, 3, kActPackedSf>(l, ka, stream)
-                           : launch_swap<16, 5, kActPackedSf>(l, ka, stream);
+    // the same tiles, stages and splits as the F8_128x4 input, so the sums are the same
+    constexpr int P = kActPackedSf;
+    if (l.T <= 16) return l.has_dependent ? launch_swap<16, 3, P>(l, ka, stream) : launch_swap<16, 5, P>(l, ka, stream);
+    if (l.T <= 32) return launch_swap<32, 5, P>(l, ka, stream);
+    if (l.T <= 64) return launch_swap<64, 4, P>(l, ka, stream);
+    if (l.T <= 128) return launch_swap<128, 6, P>(l, ka, stream);
+    if (l.T <= kSwapMaxTokens) return launch_swap<128, 3, P>(l, ka, stream);
+    if (l.n_feat % 256 == 0) return launch_pair<6, true>(l, ka, stream);
+    return launch_normal<128, 6, P>(l, ka, stream);
   }
   if (l.T <= 16) return l.has_dependent ? launch_swap<16, 3>(l, ka, stream) : launch_swap<16, 5>(l, ka, stream);
   if (l.T <= 32) return launch_swap<32, 5>(l, ka, stream);

@@ -65,7 +65,7 @@ struct GemmLaunch {
   // act is bf16 [T, act_cols] (row stride act_ld elements), quantized to MXFP8 inside the
   // kernel with mxfp8_quantize's rule; act_sf is unused. T <= 16 only.
   bool act_is_bf16;
-  // act_sf is MXQ_SF_PACKED_I32_MN (packed[w * Mp + m], Mp = ceil(T / 4) * 4). T <= 16 only.
+  // act_sf is MXQ_SF_PACKED_I32_MN (packed[w * Mp + m], Mp = ceil(T / 4) * 4), any T.
   bool act_sf_packed;
   // Optional device workspace of at least split_workspace_bytes(), zero-filled before its first
   // use; every launch that completes leaves its flags zero. With it, the CTA-pair kernel may cut
