@@ -503,9 +503,13 @@ def compact_sweep(mxq, synth, torch, dev, WA, WB):
              "roofline_us": round(o_proj_roofline_us(T, hbm, mx_tf), 2),
              "frac": round(o_proj_roofline_us(T, hbm, mx_tf) / fused, 4),
              "frac_nominal": round(o_proj_roofline_us(T, NOMINAL_HBM_GBS, NOMINAL_MXFP8_TFLOPS) / fused, 4)}
-        if T <= 16:  # bf16 o quantized inside wo_a (no quantize launch for o either)
-            r["from_bf16_us"] = round(timer(lambda: mxq.o_proj_mxfp8_from_bf16(
-                c["o"], WA, WB, T, G, NA, KA, NB, c["zq"], c["zsf"], c["out"])), 2)
+        # bf16 o quantized inside wo_a (no quantize launch for o either), against the standalone
+        # quantize launch followed by the fused pair
+        r["from_bf16_us"] = round(timer(lambda: mxq.o_proj_mxfp8_from_bf16(
+            c["o"], WA, WB, T, G, NA, KA, NB, c["zq"], c["zsf"], c["out"])), 2)
+        r["quantize_then_fused_us"] = round(timer(lambda: (
+            mxq.mxfp8_quantize(c["o"], c["oq"], None, None, c["osf"]),
+            mxq.o_proj_mxfp8(c["O"], WA, WB, T, G, NA, KA, NB, c["zq"], c["zsf"], c["out"]))), 2)
         rows.append(r)
         del c
     res["o_proj"] = rows
@@ -576,12 +580,12 @@ def sweep(args, mxq, synth, torch, dev, WA, WB):
         c = _o_proj_case(mxq, synth, torch, dev, T)
         fused, unf = _o_proj_fused_unfused(mxq, timer, c, T, WA, WB)
         extra = {}
-        if T <= 16:  # bf16 o quantized inside wo_a, against the quantize launch + the fused pair
-            extra["from_bf16_us"] = round(timer(lambda: mxq.o_proj_mxfp8_from_bf16(
-                c["o"], WA, WB, T, G, NA, KA, NB, c["zq"], c["zsf"], c["out"])), 3)
-            extra["quantize_then_fused_us"] = round(timer(lambda: (
-                mxq.mxfp8_quantize(c["o"], c["oq"], None, None, c["osf"]),
-                mxq.o_proj_mxfp8(c["O"], WA, WB, T, G, NA, KA, NB, c["zq"], c["zsf"], c["out"]))), 3)
+        # bf16 o quantized inside wo_a, against the quantize launch + the fused pair
+        extra["from_bf16_us"] = round(timer(lambda: mxq.o_proj_mxfp8_from_bf16(
+            c["o"], WA, WB, T, G, NA, KA, NB, c["zq"], c["zsf"], c["out"])), 3)
+        extra["quantize_then_fused_us"] = round(timer(lambda: (
+            mxq.mxfp8_quantize(c["o"], c["oq"], None, None, c["osf"]),
+            mxq.o_proj_mxfp8(c["O"], WA, WB, T, G, NA, KA, NB, c["zq"], c["zsf"], c["out"]))), 3)
         wa_us = timer(lambda: mxq.wo_a_einsum_mxfp8(c["O"], WA, T, G, NA, KA, z_q=c["zq"], z_sf_128x4=c["zsf"]))
         wb_us = timer(lambda: mxq.gemm_mxfp8_bf16(c["Z"], WB, c["out"]))
         roof = o_proj_roofline_us(T, hbm, mx_tf)

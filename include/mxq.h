@@ -240,18 +240,23 @@ MXQ_API mxq_status mxq_selftest_wait_timeout(int64_t limit_us, void* status, voi
 MXQ_API mxq_status mxq_selftest_hold_sms(int64_t sm_pairs, int64_t hold_us, void* stream);
 
 /*
- * o_proj_mxfp8_from_bf16 -- the _o_proj pair at decode sizes (T <= 16) fed by bf16 o
- * ([KeepMXFP8] Pieces: the small-M wo_a that quantizes its activation in the kernel, "pre-quantized
- * == in-kernel"). wo_a loads o as bf16 and quantizes each tile in shared memory with exactly the
- * rule of mxfp8_quantize, so z, its scales and out are bit-identical to mxfp8_quantize(o) followed
- * by o_proj_mxfp8; no quantize launch for o either.
+ * o_proj_mxfp8_from_bf16 -- the _o_proj pair fed by bf16 o ([KeepMXFP8] Pieces: the wo_a that
+ * quantizes its activation in the kernel, "pre-quantized == in-kernel"; Purpose: no quantize
+ * launch between the producer of o and its consumer). wo_a loads o as bf16 and quantizes each
+ * stage's tile in shared memory with exactly the rule of mxfp8_quantize (its epilogue warps, idle
+ * during the mainloop, do it), so there is no quantize launch for o either.
+ *   - T <= 384: the tiles and K splits of o_proj_mxfp8's wo_a, so z, its scales, the bf16 z and
+ *     out are bit-identical to mxfp8_quantize(o) followed by o_proj_mxfp8 (same workspace).
+ *   - T > 384: wo_a runs as 128 x 128 tiles on single SMs (not o_proj_mxfp8's SM pairs); z is
+ *     then the same up to the last bit of the bf16 rounding of some sums.
  *   o_bf16 : bf16 [T, G * Ka], row stride ld_o elements (ld_o * 2 a multiple of 16 bytes).
- * Other arguments as in o_proj_mxfp8. T > 16 returns MXQ_ERR_UNSUPPORTED_SHAPE.
+ * Other arguments as in o_proj_mxfp8 (the workspace serves wo_b).
  */
 MXQ_API mxq_status o_proj_mxfp8_from_bf16(const void* o_bf16, int64_t ld_o, const mxq_mx_tensor* wa,
                                           const mxq_mx_tensor* wb, int64_t T, int32_t G, int32_t Na, int32_t Ka,
                                           int32_t Nb, void* z_q, void* z_sf_128x4, void* z_sf_packed_i32,
-                                          void* z_bf16, void* out_bf16, void* status, void* stream);
+                                          void* z_bf16, void* out_bf16, void* workspace, int64_t workspace_bytes,
+                                          void* status, void* stream);
 
 /*
  * o_proj_mxfp8_noalloc -- o_proj_mxfp8 with the z hand-off held in a fixed buffer inside the

@@ -62,7 +62,8 @@ SIGNATURES = {
     "gemm_mxfp8_bf16": ([_MXP, _MXP, I64, I64, I64, P, I64, P, I64, P, P], ctypes.c_int),
     "o_proj_mxfp8": ([_MXP, _MXP, _MXP, I64, I32, I32, I32, I32, P, P, P, P, P, P, I64, P, P], ctypes.c_int),
     "o_proj_mxfp8_noalloc": ([_MXP, _MXP, _MXP, I64, I32, I32, I32, I32, P, P, P], ctypes.c_int),
-    "o_proj_mxfp8_from_bf16": ([P, I64, _MXP, _MXP, I64, I32, I32, I32, I32, P, P, P, P, P, P, P], ctypes.c_int),
+    "o_proj_mxfp8_from_bf16": ([P, I64, _MXP, _MXP, I64, I32, I32, I32, I32, P, P, P, P, P, P, I64, P, P],
+                               ctypes.c_int),
 }
 
 # capacity of the library-held z buffer of o_proj_mxfp8_noalloc (include/mxq.h)
@@ -250,13 +251,15 @@ def o_proj_mxfp8_noalloc(o: MXFP8, wa: MXFP8, wb: MXFP8, T: int, G: int, Na: int
 
 def o_proj_mxfp8_from_bf16(o: torch.Tensor, wa: MXFP8, wb: MXFP8, T: int, G: int, Na: int, Ka: int, Nb: int, z_q,
                            z_sf_128x4, out: torch.Tensor, z_sf_packed=None, z_bf16=None, status=None,
-                           stream=None) -> None:
-    """The _o_proj pair from bf16 o (T <= 16): wo_a quantizes o in the kernel."""
+                           stream=None, workspace=None) -> None:
+    """The _o_proj pair from bf16 o: wo_a quantizes o in the kernel (no quantize launch).
+    workspace: None = the stream's own split workspace, False = none, or a tensor."""
     assert o.dtype == torch.bfloat16 and o.dim() == 2 and o.stride(1) == 1
     ac, bc = wa.c(), wb.c()
+    wp, wn = _ws(workspace, stream)
     _check(load().o_proj_mxfp8_from_bf16(_ptr(o), o.stride(0), ctypes.byref(ac), ctypes.byref(bc), T, G, Na, Ka, Nb,
                                          _ptr(z_q), _ptr(z_sf_128x4), _ptr(z_sf_packed), _ptr(z_bf16), _ptr(out),
-                                         _ptr(status), _stream(stream)), "o_proj_mxfp8_from_bf16")
+                                         wp, wn, _ptr(status), _stream(stream)), "o_proj_mxfp8_from_bf16")
 
 
 def selftest_wait_timeout(limit_us: int, status: torch.Tensor, stream=None) -> None:

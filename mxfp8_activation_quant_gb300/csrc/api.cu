@@ -286,11 +286,11 @@ mxq_status o_proj_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, const m
 
 mxq_status o_proj_mxfp8_from_bf16(const void* o_bf16, int64_t ld_o, const mxq_mx_tensor* wa, const mxq_mx_tensor* wb,
                                   int64_t T, int32_t G, int32_t Na, int32_t Ka, int32_t Nb, void* z_q,
-                                  void* z_sf_128x4, void* z_sf_packed_i32, void* z_bf16, void* out_bf16, void* status,
-                                  void* stream) {
+                                  void* z_sf_128x4, void* z_sf_packed_i32, void* z_bf16, void* out_bf16,
+                                  void* workspace, int64_t workspace_bytes, void* status, void* stream) {
   if (o_bf16 == nullptr || z_q == nullptr || z_sf_128x4 == nullptr || out_bf16 == nullptr) return MXQ_ERR_INVALID_ARG;
   if (T <= 0 || G <= 0 || Na <= 0 || Ka <= 0 || Nb <= 0) return MXQ_ERR_INVALID_ARG;
-  if (T > 16 || Na % 128 != 0 || Ka % 128 != 0 || Nb % 128 != 0) return MXQ_ERR_UNSUPPORTED_SHAPE;
+  if (Na % 128 != 0 || Ka % 128 != 0 || Nb % 128 != 0 || T >= (int64_t(1) << 31)) return MXQ_ERR_UNSUPPORTED_SHAPE;
   const int64_t Ko = static_cast<int64_t>(G) * Ka, Kb = static_cast<int64_t>(G) * Na;
   if (ld_o < Ko || Ko >= (int64_t(1) << 31) || Kb >= (int64_t(1) << 31)) return MXQ_ERR_UNSUPPORTED_SHAPE;
   mxq_status st = check_operand(wa, Kb, Ka);
@@ -299,6 +299,7 @@ mxq_status o_proj_mxfp8_from_bf16(const void* o_bf16, int64_t ld_o, const mxq_mx
   if (!al16(o_bf16) || (ld_o * 2) % 16 != 0 || !al16(z_q) || !al16(z_sf_128x4) || !al16(z_sf_packed_i32) ||
       !al16(z_bf16) || !al16(out_bf16) || !al16(status))
     return MXQ_ERR_MISALIGNED;
+  if ((st = check_workspace(workspace, workspace_bytes)) != MXQ_OK) return st;
   mxq::GemmLaunch l = {};
   l.act = o_bf16;
   l.act_cols = Ko;
@@ -322,7 +323,7 @@ mxq_status o_proj_mxfp8_from_bf16(const void* o_bf16, int64_t ld_o, const mxq_mx
   st = from_cuda(mxq::launch_gemm(l, static_cast<cudaStream_t>(stream)));
   if (st != MXQ_OK) return st;
   const mxq_mx_tensor z = {z_q, z_sf_128x4, MXQ_SF_TILED_128X4, T, Kb, Kb};
-  return gemm_impl(&z, wb, T, Nb, Kb, out_bf16, Nb, nullptr, 0, status, stream, true);
+  return gemm_impl(&z, wb, T, Nb, Kb, out_bf16, Nb, workspace, workspace_bytes, status, stream, true);
 }
 
 mxq_status mxq_selftest_wait_timeout(int64_t limit_us, void* status, void* stream) {

@@ -98,13 +98,17 @@ struct Cfg {
   // scale atom before the MMAs of the stage. kActPackedSf: the activation tile arrives as usual
   // and the stage's packed scale words (one per token row of the tile) land in the staging slot,
   // which the epilogue warps scatter into the activation's F8_128x4 atom.
+  // (in the normal orientation the activation is A, 128 rows: used with BN = 128 only)
   static constexpr int BF_BYTES = ACT == kActBf16 ? BN * 256 : ACT == kActPackedSf ? BN * 4 : 0;
   // bytes on the stage's full barrier; the staged activation part has a barrier of its own, so
   // its conversion starts as soon as it lands, under the larger weight load
   static constexpr int TX_BYTES = ACT == kActBf16 ? A_BYTES + 512 : ACT == kActPackedSf ? A_BYTES + B_BYTES + 512
                                                                                        : A_BYTES + B_BYTES + SF_BYTES;
   static constexpr int OFF_B = STAGES * A_BYTES;
-  static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
+  // staging slots right behind the operand tiles, so that the split-K exchange below (after the
+  // mainloop) may use them too
+  static constexpr int OFF_BF = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_SF = OFF_BF + STAGES * BF_BYTES;
   // Split-K reduction (swap-AB). Token tiles of 16 columns (decode) push their partials
   // with per-thread st.async into a dedicated receive buffer [source rank][feature][column] as
   // soon as their own MMAs are done (PUSH). Wider tiles stage their partials in the operand
@@ -114,8 +118,7 @@ struct Cfg {
   static constexpr bool PUSH = BN <= 16;
   static constexpr int RECV_BYTES = PUSH ? 128 * BN * 4 : 0;
   static constexpr bool split_fits(int s) { return PUSH || BN * 512 + BN * 512 / s * (s - 1) <= OFF_SF; }
-  static constexpr int OFF_BF = OFF_SF + STAGES * SF_BYTES;
-  static constexpr int OFF_RECV = OFF_BF + STAGES * BF_BYTES;
+  static constexpr int OFF_RECV = OFF_SF + STAGES * SF_BYTES;
   static constexpr int OFF_BAR = OFF_RECV + RECV_BYTES;
   // full, empty, 4 more, and (ACT != kActMx) "converted" and "staged part landed" per stage
   static constexpr int OFF_MISC = OFF_BAR + ((ACT != kActMx ? 4 : 2) * STAGES + 4) * 8;
@@ -284,9 +287,9 @@ template <int BN, int STAGES, bool SWAP, int ACT = kActMx, int US = 0>
 __global__ void __launch_bounds__(kThreads, 3)
     gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                      const KArgs p) {
-  static_assert(ACT == kActMx || ACT == kActPackedSf || (SWAP && BN == 16), "bf16 activations: decode tiles only");
+  static_assert(ACT != kActBf16 || (SWAP ? BN <= 128 : BN == BM), "bf16 activations: one 128-row staging slot");
   static_assert(ACT != kActPackedSf || BN <= 128, "packed activation scales: one activation atom per stage");
-  static_assert(US == 0 || (SWAP && ACT != kActBf16 && BN >= 32 && US <= BN / 4), "uneven split: wide tiles");
+  static_assert(US == 0 || (SWAP && BN >= 32 && US <= BN / 4), "uneven split: wide tiles");
   constexpr bool CVT = ACT != kActMx;  // a staged activation part converted by the epilogue warps
   using C = Cfg<BN, STAGES, ACT>;
   extern __shared__ uint8_t smem_raw[];
@@ -371,6 +374,11 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
       for (int j = 0; j < C::SFB_ATOMS; ++j)
         bulk_load(sf_dst0 + s * C::SF_BYTES + 512 * (1 + j), b_sf + ((b_rt0 + j) * b_gp4 + b_kc0 + kb) * 512, 512, fb);
+    } else if (ACT == kActBf16) {  // normal orientation, bf16 activations (128 token rows)
+      const uint32_t ab = bar_act + (fb - bar_full);
+      mbar_arrive_expect_tx(ab, C::BF_BYTES);
+      tma_load_2d(sbase + C::OFF_BF + s * C::BF_BYTES, &tm_a, ab, static_cast<int32_t>(a_xoff + kb * BK),
+                  static_cast<int32_t>(a_row0));
     } else if (ACT == kActPackedSf) {  // normal orientation: the activation is A (128 token rows)
       tma_load_2d(a_dst0 + s * C::A_BYTES, &tm_a, fb, static_cast<int32_t>(a_xoff + kb * BK), static_cast<int32_t>(a_row0));
       const uint32_t ab = bar_act + (fb - bar_full);
@@ -539,14 +547,21 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
   if (ACT == kActBf16 && epi) {
     // During the mainloop the epilogue warps quantize each stage's bf16 activations exactly as
-    // mxfp8_quantize does: thread t takes token row t / 8 and 16 elements of group (t / 2) % 4;
-    // the two halves of a group meet by one shuffle for the amax.
+    // mxfp8_quantize does, into the activation tile (128-byte swizzle) and its F8_128x4 atom: a
+    // unit is 16 elements (half a group) of one token row, thread t takes row t / 8 + 16 i and
+    // half h = t % 2 of group (t / 2) % 4; the two halves of a group meet by one shuffle for the
+    // amax. Rows past the last token arrive as zeros (the copy's fill) and get scale 0.
+    constexpr int ROWS = SWAP ? BN : BM;
     const int t = static_cast<int>(threadIdx.x) - 64;
-    const int r = t >> 3, c = (t >> 1) & 3, h = t & 1;
-    // rows >= 16 of the activation scale atoms stay zero
-    for (int i = t; i < STAGES * 128; i += 128)
-      reinterpret_cast<uint32_t*>(smem + C::OFF_SF + (i >> 7) * C::SF_BYTES + 512)[i & 127] = 0u;
-    named_barrier(3, 128);
+    const int c = (t >> 1) & 3, h = t & 1;
+    const uint32_t tile0 = SWAP ? sbase + C::OFF_B : sbase;
+    const int tile_bytes = SWAP ? C::B_BYTES : C::A_BYTES;
+    const int atom = SWAP ? C::ACT_ATOM : 0;
+    if (ROWS < 128) {  // atom rows past the tile's stay zero
+      for (int i = t; i < STAGES * 128; i += 128)
+        reinterpret_cast<uint32_t*>(smem + C::OFF_SF + (i >> 7) * C::SF_BYTES + atom)[i & 127] = 0u;
+      named_barrier(3, 128);
+    }
     for (int i = 0; i < nk; ++i) {
       const int s = i % STAGES;
       if (!mbar_wait_bounded(bar_act + 8 * s, (i / STAGES) & 1)) {
@@ -554,16 +569,20 @@ __global__ void __launch_bounds__(kThreads, 3)
         report_timeout(p.status);
         break;
       }
-      const uint4* src = reinterpret_cast<const uint4*>(smem + C::OFF_BF + s * C::BF_BYTES + r * 256 + (32 * c + 16 * h) * 2);
-      const uint4 v0 = src[0], v1 = src[1];
-      uint32_t am = max(absmax8(v0), absmax8(v1));
-      am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
-      const uint32_t code = ue8m0_from_bf16_amax(am);
-      const float sc = ue8m0_inverse(code);
-      const uint2 q0 = quant8(v0, sc), q1 = quant8(v1, sc);
-      const int j = 2 * c + h;  // 16-byte chunk of the 128-byte row, 128-byte swizzle
-      st_smem_v4(sbase + C::OFF_B + s * C::B_BYTES + r * 128 + ((j ^ (r & 7)) << 4), q0.x, q0.y, q1.x, q1.y);
-      if (h == 0) smem[C::OFF_SF + s * C::SF_BYTES + 512 + r * 16 + c] = static_cast<uint8_t>(code);
+#pragma unroll
+      for (int u = 0; u < ROWS / 16; ++u) {
+        const int r = (t >> 3) + 16 * u;
+        const uint4* src = reinterpret_cast<const uint4*>(smem + C::OFF_BF + s * C::BF_BYTES + r * 256 + (32 * c + 16 * h) * 2);
+        const uint4 v0 = src[0], v1 = src[1];
+        uint32_t am = max(absmax8(v0), absmax8(v1));
+        am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
+        const uint32_t code = ue8m0_from_bf16_amax(am);
+        const float sc = ue8m0_inverse(code);
+        const uint2 q0 = quant8(v0, sc), q1 = quant8(v1, sc);
+        const int j = 2 * c + h;  // 16-byte chunk of the 128-byte row, 128-byte swizzle
+        st_smem_v4(tile0 + s * tile_bytes + r * 128 + ((j ^ (r & 7)) << 4), q0.x, q0.y, q1.x, q1.y);
+        if (h == 0) smem[C::OFF_SF + s * C::SF_BYTES + atom + (r & 31) * 16 + (r >> 5) * 4 + c] = static_cast<uint8_t>(code);
+      }
       fence_proxy_async_smem();  // the MMA and the scale copy read these through the async proxy
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_conv + 8 * s);
@@ -1532,7 +1551,7 @@ cudaError_t launch_cfg(const GemmLaunch& l, const KArgs& ka, dim3 grid, int clus
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap tma_act, tma_wt;
   if (ACT == kActBf16) {
-    if (!make_bf16_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, BN)) return cudaErrorInvalidValue;
+    if (!make_bf16_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, SWAP ? BN : BM)) return cudaErrorInvalidValue;
   } else if (!make_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, SWAP ? BN : BM)) {
     return cudaErrorInvalidValue;
   }
@@ -1600,22 +1619,38 @@ int uneven_clusters_resident() {
   return n;
 }
 
-template <int BN, int STAGES, int ACT = kActMx>
-cudaError_t launch_swap(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
-  const int tok_tiles = static_cast<int>(ceil_div(l.T, BN));
-  const int tiles = l.G * (l.n_feat / BM) * tok_tiles;
-  const int kb_total = l.k_len / BK;
-  const int slots = num_sms() * ctas_per_sm<BN, STAGES, ACT>();
-  const int s = pick_splits<BN, STAGES, ACT>(tiles, kb_total, slots);
+// The split of K (cluster size) that the MXFP8-input configuration <BN, PLAN> chooses; the
+// packed-scale and bf16-input variants take the same one, so that every output sums the same
+// partial products in the same order as with MXFP8 input.
+template <int BN, int PLAN>
+int plan_splits(int tiles, int kb_total) {
+  const int slots = num_sms() * ctas_per_sm<BN, PLAN>();
+  const int s = pick_splits<BN, PLAN>(tiles, kb_total, slots);
   // The one-CTA-per-SM band (128-token tiles, 6 stages): when the power-of-two split leaves SMs
   // idle and 3 ranks of every tile still fit in one wave, K is cut over 3 ranks. The gate is on
   // the tile and SM counts, not on the operand: at the DeepSeek-V4.1 shapes wo_b (40 tiles: 80
   // CTAs -> 120) takes it, while wo_a (64 tiles: 3 ranks would need 192 CTAs) stays on two.
-  if constexpr (BN == 128 && STAGES == 6 && ACT != kActBf16) {
+  if constexpr (BN == 128 && PLAN == 6) {
+    constexpr int US = 3;
+    constexpr bool fits = BN * 512 + 2048 * ((BN / 4 + US - 1) / US) * (US - 1) <= Cfg<BN, PLAN>::OFF_SF;
+    if (fits && s < US && tiles * s < num_sms() && tiles * US <= slots && kb_total >= 2 * US &&
+        tiles <= uneven_clusters_resident<BN, PLAN, US, kActMx>())
+      return US;
+  }
+  return s;
+}
+
+template <int BN, int STAGES, int ACT = kActMx, int PLAN = STAGES>
+cudaError_t launch_swap(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
+  const int tok_tiles = static_cast<int>(ceil_div(l.T, BN));
+  const int tiles = l.G * (l.n_feat / BM) * tok_tiles;
+  const int kb_total = l.k_len / BK;
+  int s = plan_splits<BN, PLAN>(tiles, kb_total);
+  if constexpr (BN == 128) {
     constexpr int US = 3;
     constexpr bool fits = BN * 512 + 2048 * ((BN / 4 + US - 1) / US) * (US - 1) <= Cfg<BN, STAGES, ACT>::OFF_SF;
-    if (fits && s < US && tiles * s < num_sms() && tiles * US <= slots && kb_total >= 2 * US &&
-        tiles <= uneven_clusters_resident<BN, STAGES, US, ACT>()) {
+    if (s == US && !fits) s = 2;  // (a configuration with less staging room: the nearest split that fits)
+    if (s == US) {
       ka.splits = US;
       ka.kb_per_cta = kb_total;  // all k-blocks: the kernel cuts the uneven ranges
       ka.per_rank_shift = 0;
@@ -1623,6 +1658,7 @@ cudaError_t launch_swap(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
       return launch_cfg<BN, STAGES, true, ACT, US>(l, ka, grid, US, stream);
     }
   }
+  while (s > 1 && (!Cfg<BN, STAGES, ACT>::split_fits(s) || kb_total % s != 0 || BN / s < 4)) s >>= 1;
   ka.splits = s;
   ka.kb_per_cta = kb_total / s;
   ka.per_rank_shift = 0;
@@ -1785,9 +1821,17 @@ cudaError_t launch_gemm(const GemmLaunch& l, cudaStream_t stream) {
   // T <= 16: a grid followed by a dependent (wo_a of o_proj_mxfp8) uses 3 stages so that the
   // dependent wo_b CTAs that find room start early and fetch their first weight stages; other
   // grids keep 5 stages, about 14 MB of loads in flight
-  if (l.act_is_bf16) {  // bf16 activations, quantized in the kernel: decode tiles only
-    if (l.T > 16) return cudaErrorInvalidValue;
-    return launch_swap<16, 3, kActBf16>(l, ka, stream);
+  if (l.act_is_bf16) {
+    // bf16 activations, quantized in the kernel (wo_a of o_proj_mxfp8_from_bf16: a grid that a
+    // dependent wo_b follows). The staging slots leave room for fewer stages; the splits are
+    // those of the MXFP8-input configuration of the same band.
+    constexpr int B = kActBf16;
+    if (l.T <= 16) return launch_swap<16, 3, B>(l, ka, stream);
+    if (l.T <= 32) return launch_swap<32, 3, B, 5>(l, ka, stream);
+    if (l.T <= 64) return launch_swap<64, 2, B, 4>(l, ka, stream);
+    if (l.T <= 128) return launch_swap<128, 3, B, 6>(l, ka, stream);
+    if (l.T <= kSwapMaxTokens) return launch_swap<128, 3, B, 3>(l, ka, stream);
+    return launch_normal<128, 3, B>(l, ka, stream);
   }
   if (l.act_sf_packed) {  // int32-packed activation scales, moved into atoms in the kernel
     // the same tiles, stages and splits as the F8_128x4 input, so the sums are the same

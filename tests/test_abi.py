@@ -135,11 +135,13 @@ def test_o_proj_from_bf16_argument_errors(lib):
     B = ctypes.byref
     f = lib.o_proj_mxfp8_from_bf16
     args = (B(mx(8192, 4096)), B(mx(5120, 8192)))
-    assert f(FAKE, 32768, *args, 17, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, None, None) == 2  # T > 16
-    assert f(None, 32768, *args, 4, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, None, None) == 1
-    assert f(FAKE, 32000, *args, 4, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, None, None) == 2  # ld_o
-    assert f(FAKE + 2, 32768, *args, 4, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, None, None) == 3
-    assert f(FAKE, 32772, *args, 4, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, None, None) == 3  # ld_o*2 % 16
+    ws = (None, 0)
+    assert f(FAKE, 32768, *args, 4, 8, 1000, 4096, 5120, FAKE, FAKE, None, None, FAKE, *ws, None, None) == 2  # Na
+    assert f(None, 32768, *args, 4, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, *ws, None, None) == 1
+    assert f(FAKE, 32000, *args, 4, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, *ws, None, None) == 2  # ld_o
+    assert f(FAKE + 2, 32768, *args, 4, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, *ws, None, None) == 3
+    assert f(FAKE, 32772, *args, 4, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, *ws, None, None) == 3  # ld_o*2 % 16
+    assert f(FAKE, 32768, *args, 4, 8, 1024, 4096, 5120, FAKE, FAKE, None, None, FAKE, FAKE, 16, None, None) == 1  # ws size
 
 
 def test_selftest_argument_errors(lib):

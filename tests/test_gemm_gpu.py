@@ -498,12 +498,16 @@ def test_fused_chain_launches_two_kernels(mxq, weights, T):
     assert _kernel_nodes(g2) == (3, 3)
 
 
-@pytest.mark.parametrize("T,pad", [(1, 0), (2, 0), (4, 0), (7, 64), (16, 0)])
+@pytest.mark.parametrize("T,pad", [(1, 0), (2, 0), (4, 0), (7, 64), (16, 0), (17, 0), (33, 64), (100, 0), (129, 0),
+                                   (256, 0), (300, 64), (384, 0), (385, 0), (1000, 64), (4096, 0), (8193, 0)])
 def test_o_proj_from_bf16_matches_prequantized(mxq, oracle, weights, T, pad):
-    """wo_a quantizing bf16 o in the kernel gives the same bytes as mxfp8_quantize(o) followed
-    by o_proj_mxfp8: z, both scale layouts, the bf16 z and out (the pages' "pre-quantized ==
-    in-kernel"); and the in-kernel path on its own meets the oracle chain's tolerances (bf16 z
-    within 4e-3, out within 1e-2). `pad` extra columns make o a strided view."""
+    """wo_a quantizing bf16 o in the kernel against mxfp8_quantize(o) followed by o_proj_mxfp8
+    (the pages' "pre-quantized == in-kernel"). Up to 384 tokens both run the same tiles and K
+    splits: z, both scale layouts, the bf16 z and out are the same bytes. Beyond, wo_a runs on
+    single SMs instead of SM pairs: the bf16 z may differ by one rounding of a sum, and the fused
+    MXFP8 z is still the quantizer's output on this call's bf16 z. Either way the in-kernel path
+    meets the oracle chain's tolerances (bf16 z within 4e-3, out within 1e-2; sampled rows beyond
+    384 tokens). `pad` extra columns make o a strided view."""
     from mxfp8_activation_quant_gb300 import synth
 
     o_full = torch.zeros((T, synth.G * synth.KA + pad), dtype=torch.bfloat16, device="cuda")
@@ -525,11 +529,20 @@ def test_o_proj_from_bf16_matches_prequantized(mxq, oracle, weights, T, pad):
                      z_sf_packed=b[2], z_bf16=b[3], status=st)
     torch.cuda.synchronize()
     mxq.check_status(st)
-    for x, y in zip(a, b):
-        assert torch.equal(x, y)
-    z_ref, out_ref = oracle_chain(oracle, weights, bf16_bits(o))
-    assert rel_fro(bits_to_f64(bf16_bits(a[3])), z_ref) <= 4e-3
-    assert rel_fro(bits_to_f64(bf16_bits(a[4])), out_ref) <= 1e-2
+    if T <= 384:
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+    else:
+        za, zb = a[3].float(), b[3].float()
+        assert bool(((za - zb).abs() <= zb.abs() * 2.0 ** -7).all())  # at most one bf16 rounding step
+        q2, sfs = mxq.quantize(a[3], layouts=(1, 2))
+        torch.cuda.synchronize()
+        assert torch.equal(q2, a[0]) and torch.equal(sfs[2], a[1]) and torch.equal(sfs[1], a[2])
+    rows = np.arange(T) if T <= 384 else synth.sample_rows(0, T).numpy()
+    o_rows = o.cpu()[torch.from_numpy(rows)]
+    z_ref, out_ref = oracle_chain(oracle, weights, bf16_bits(o_rows))
+    assert rel_fro(bits_to_f64(bf16_bits(a[3]))[rows], z_ref) <= 4e-3
+    assert rel_fro(bits_to_f64(bf16_bits(a[4]))[rows], out_ref) <= 1e-2
 
 
 @pytest.mark.parametrize("T,N,K", [(1, 256, 512), (17, 256, 512), (40, 128, 1024), (100, 5120, 8192),
