@@ -1282,6 +1282,12 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       int t, g, nf, kb_lo, kb_hi;
       int64_t m0, n0;
       if (!seg(w, t, g, m0, n0, nf, kb_lo, kb_hi)) break;
+      // A tile of the split tail shared with another pair: take the tile's arrival ticket now,
+      // while this segment's MMAs run, so that its latency stays off the epilogue's path (holding
+      // a ticket means running, which is all the last holder relies on; see below).
+      const bool split_seg = sk && (kb_lo > 0 || kb_hi < nk) && m0 + BM * rank < p.z_mp128 && 128 * half < nf;
+      int arrived = 0;
+      if (split_seg && lane == 0) arrived = atomicAdd(p.sk_ticket + ((t - tail0) * 2 + static_cast<int>(rank)) * 8 + ew, 1);
       if (!mbar_wait_bounded(bar_accf, ti & 1)) {
         *abort_flag = 1;
         report_timeout(p.status);
@@ -1305,12 +1311,12 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       // contiguous and each of its 16-byte stores or loads covers 512 contiguous bytes. Rows past
       // the last token hold zeros on every side and are neither stored nor loaded.
       const bool live = row < p.T;
-      if (sk && (kb_lo > 0 || kb_hi < nk) && row0 < p.z_mp128) {
+      if (split_seg) {
         // A tile of the split tail shared with other pairs: its k-blocks lie in the consecutive
-        // ranges of pairs [q_lo, q_hi). Every sharer takes a ticket once its MMAs are done; the
-        // last to arrive finishes the tile, the others store their partial sums and raise their
+        // ranges of pairs [q_lo, q_hi). Every sharer takes a ticket when its segment starts; the
+        // last to do so finishes the tile, the others store their partial sums and raise their
         // flag. So nobody waits for a pair that has not started: the finisher waits only for
-        // sharers that already hold a ticket and are storing.
+        // sharers that already hold a ticket, whose MMAs need nothing from anyone.
         const int tt = t - tail0;
         const int64_t k_lo = static_cast<int64_t>(tt) * nk, k_hi = k_lo + nk;
         int q_lo = pair, q_hi = pair + 1;
@@ -1325,8 +1331,6 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         int sharers = 0;
         for (int qq = q_lo; qq < q_hi; ++qq) sharers += range_lo(qq + 1) > range_lo(qq) ? 1 : 0;
         int32_t* ticket = p.sk_ticket + (tt * 2 + static_cast<int>(rank)) * 8 + ew;
-        int arrived = 0;
-        if (lane == 0) arrived = atomicAdd(ticket, 1);
         arrived = __shfl_sync(0xffffffffu, arrived, 0);
         if (arrived == sharers - 1) {
           bool ok = true;
