@@ -17,8 +17,11 @@
 namespace mxq {
 namespace {
 
-constexpr int kUnits = 4;  // 256-column units per warp
 constexpr int kWarpsPerBlock = 4;  // 128-thread blocks: about 1 % faster than 256 at every measured size
+// 256-column units per warp: 4 (16 KB of loads in flight per block) from 8 M elements up, 2 below
+// (more, smaller blocks: [256, 8192] 4.18 -> 3.72 us, [1024, 8192] 7.50 -> 7.19 us; at
+// [32768, 8192] 2 units lose 10 %)
+constexpr int64_t kSmallQuantElems = int64_t(8) << 20;
 constexpr int64_t kEarlyGammaRows = 256;  // RMSNorm row counts that load gamma early (measured)
 
 struct QuantArgs {
@@ -52,6 +55,7 @@ __device__ __forceinline__ void store_unit_scales(const QuantArgs& a, int64_t ro
 
 // at least 12 blocks per SM (40 registers): 75 % occupancy instead of 62.5 %, 1-2 % faster at
 // large sizes (16 blocks forces spills and is slower)
+template <int kUnits>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, 12) quantize_kernel(const QuantArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t wid = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -80,8 +84,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 12) quantize_kernel(const
 }
 
 // ------------------------------------------------------------------------------------------
-// RMSNorm with bf16 + MXFP8 outputs. One 128-thread block per row; thread t owns the 8-element
-// chunks t, t + 128, ... of the row (CPT of them), held in registers between the two phases.
+// RMSNorm with bf16 + MXFP8 outputs. One block of NT threads per row; thread t owns the
+// 8-element chunks t, t + NT, ... of the row (CPT of them), held in registers between the two
+// phases. NT is a multiple of 16, so a scale word's 16 chunks stay in 16 lanes of one warp.
+// Measured at H = 5120 (cold-L2 graph timing): 256 threads are fastest up to 512 rows (T = 512:
+// 6.35 -> 5.57 us), 160 (one group per thread) up to 2048 (T = 1024: 7.91 -> 7.49 us), 128 beyond.
 // ------------------------------------------------------------------------------------------
 struct RmsArgs {
   const uint16_t* x;
@@ -99,19 +106,19 @@ struct RmsArgs {
 // EARLY_G: load gamma with x instead of after the reduction. It removes one memory round trip
 // from a block's critical path, which is the whole kernel when there are few rows; with many
 // rows its extra registers cost more residency than it saves.
-template <int CPT, bool EARLY_G>
-__global__ void __launch_bounds__(128) rmsnorm_dual_kernel(const RmsArgs a) {
+template <int CPT, bool EARLY_G, int NT>
+__global__ void __launch_bounds__(NT) rmsnorm_dual_kernel(const RmsArgs a) {
   const int64_t row = blockIdx.x;
   if (row >= a.rows_total) return;  // block-uniform
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool vrow = row < a.T;
-  __shared__ float red[4];
+  __shared__ float red[NT / 32];
 
   uint4 v[CPT], gv[CPT];
   float ss = 0.f;
 #pragma unroll
   for (int j = 0; j < CPT; ++j) {
-    const int64_t c = 8 * (tid + 128 * j);
+    const int64_t c = 8 * (tid + NT * j);
     v[j] = (vrow && c < a.H) ? ld_stream_u4(a.x + row * a.ldx + c) : make_uint4(0, 0, 0, 0);
     if (EARLY_G) gv[j] = (vrow && c < a.H) ? *reinterpret_cast<const uint4*>(a.gamma + c) : make_uint4(0, 0, 0, 0);
     const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
@@ -126,7 +133,9 @@ __global__ void __launch_bounds__(128) rmsnorm_dual_kernel(const RmsArgs a) {
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if (lane == 0) red[warp] = ss;
   __syncthreads();
-  const float total = (red[0] + red[1]) + (red[2] + red[3]);
+  float total = 0.f;
+#pragma unroll
+  for (int k = 0; k < NT / 32; ++k) total += red[k];
   const float r = rsqrtf(total / a.h + a.eps);
 
   QuantArgs qa;
@@ -142,9 +151,9 @@ __global__ void __launch_bounds__(128) rmsnorm_dual_kernel(const RmsArgs a) {
 
 #pragma unroll
   for (int j = 0; j < CPT; ++j) {
-    const int64_t cbase = static_cast<int64_t>(8) * 128 * j;
+    const int64_t cbase = static_cast<int64_t>(8) * NT * j;
     if (cbase >= a.H) break;  // block-uniform
-    const int64_t c = 8 * (tid + 128 * j);
+    const int64_t c = 8 * (tid + NT * j);
     uint4 y = make_uint4(0, 0, 0, 0);
     if (vrow && c < a.H) {
       const uint4 g = EARLY_G ? gv[j] : *reinterpret_cast<const uint4*>(a.gamma + c);
@@ -163,13 +172,29 @@ __global__ void __launch_bounds__(128) rmsnorm_dual_kernel(const RmsArgs a) {
   }
 }
 
-template <int CPT>
+template <int CPT, int NT>
 cudaError_t launch_rms_cpt(const RmsArgs& ra, cudaStream_t stream) {
   if (ra.rows_total <= kEarlyGammaRows)
-    rmsnorm_dual_kernel<CPT, true><<<static_cast<unsigned>(ra.rows_total), 128, 0, stream>>>(ra);
+    rmsnorm_dual_kernel<CPT, true, NT><<<static_cast<unsigned>(ra.rows_total), NT, 0, stream>>>(ra);
   else
-    rmsnorm_dual_kernel<CPT, false><<<static_cast<unsigned>(ra.rows_total), 128, 0, stream>>>(ra);
+    rmsnorm_dual_kernel<CPT, false, NT><<<static_cast<unsigned>(ra.rows_total), NT, 0, stream>>>(ra);
   return cudaGetLastError();
+}
+
+template <int NT>
+cudaError_t launch_rms_nt(const RmsArgs& ra, int64_t H, cudaStream_t stream) {
+  switch ((H / 8 + NT - 1) / NT) {  // 8-element chunks per thread
+    case 1: return launch_rms_cpt<1, NT>(ra, stream);
+    case 2: return launch_rms_cpt<2, NT>(ra, stream);
+    case 3: return launch_rms_cpt<3, NT>(ra, stream);
+    case 4: return launch_rms_cpt<4, NT>(ra, stream);
+    case 5: return launch_rms_cpt<5, NT>(ra, stream);
+    case 6: return launch_rms_cpt<6, NT>(ra, stream);
+    case 7: case 8: return launch_rms_cpt<8, NT>(ra, stream);
+    case 9: case 10: case 11: case 12: return launch_rms_cpt<12, NT>(ra, stream);
+    case 13: case 14: case 15: case 16: return launch_rms_cpt<16, NT>(ra, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -192,11 +217,16 @@ cudaError_t launch_quantize(const QuantizeLaunch& l, cudaStream_t stream) {
   a.Mp4 = ceil_div(l.M, 4) * 4;
   a.Mp128 = ceil_div(l.M, 128) * 128;
   a.rows_total = a.sf_tl ? a.Mp128 : (a.sf_pk ? a.Mp4 : l.M);
-  a.chunks = static_cast<int32_t>(ceil_div(l.K, 256 * kUnits));
+  const bool small = l.M * l.K <= kSmallQuantElems;
+  const int units = small ? 2 : 4;
+  a.chunks = static_cast<int32_t>(ceil_div(l.K, 256 * units));
   const int64_t warps = a.rows_total * a.chunks;
   const int64_t blocks = ceil_div(warps, kWarpsPerBlock);
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  quantize_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a);
+  if (small)
+    quantize_kernel<2><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a);
+  else
+    quantize_kernel<4><<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -220,19 +250,9 @@ cudaError_t launch_rmsnorm(const RmsnormLaunch& l, cudaStream_t stream) {
   a.Mp128 = ceil_div(l.T, 128) * 128;
   a.rows_total = a.sf_tl ? a.Mp128 : (a.sf_pk ? a.Mp4 : l.T);
   if (a.rows_total > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  const int64_t cpt = ceil_div(ceil_div(l.H, 8), 128);
-  switch (cpt) {
-    case 1: return launch_rms_cpt<1>(a, stream);
-    case 2: return launch_rms_cpt<2>(a, stream);
-    case 3: return launch_rms_cpt<3>(a, stream);
-    case 4: return launch_rms_cpt<4>(a, stream);
-    case 5: return launch_rms_cpt<5>(a, stream);
-    case 6: return launch_rms_cpt<6>(a, stream);
-    case 7: case 8: return launch_rms_cpt<8>(a, stream);
-    case 9: case 10: case 11: case 12: return launch_rms_cpt<12>(a, stream);
-    case 13: case 14: case 15: case 16: return launch_rms_cpt<16>(a, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  if (a.rows_total <= 512) return launch_rms_nt<256>(a, l.H, stream);
+  if (a.rows_total <= 2048) return launch_rms_nt<160>(a, l.H, stream);
+  return launch_rms_nt<128>(a, l.H, stream);
 }
 
 }  // namespace mxq
