@@ -210,6 +210,68 @@ __device__ __forceinline__ void epi_row_chunk(const KArgs& p, const uint32_t (&a
   }
 }
 
+// normal orientation through a warp's 2 KB staging block (CTA-pair kernel): lane l holds token
+// row row0 + l and 32 consecutive feature columns. The warp writes the chunk back row by row, so
+// that one store instruction covers 8 rows x 64 bytes (bf16) or 16 rows x 32 bytes (E4M3): whole
+// 32-byte sectors, a quarter of the requests of a 16-byte piece in each of 32 rows. Measured in
+// cold-L2 graph replay: the _o_proj pair at 512 tokens 52.0 -> 49.3 us, at 2048 122.2 -> 117.9 us,
+// at 4096 208.4 -> 203.3 us (with the stores removed altogether wo_b at 4096 tokens would take
+// 107.6 instead of 114.5 us: the scattered pieces drained slowly in the exposed last tile). Staging
+// a warp's whole 32 x 128 share of the last tile in the idle operand stages, for 128- and 256-byte
+// rows, was no faster. The 16-byte pieces of a staged row are XOR-swizzled by the row, so that
+// neither the staging stores nor the loads conflict on banks. Every lane of the warp calls it.
+__device__ __forceinline__ void epi_row_chunk_staged(const KArgs& p, const uint32_t (&acc)[32], int64_t row0, int lane,
+                                                     int64_t col, uint32_t& word, int c, uint32_t stage) {
+  uint32_t hb[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) hb[i] = bf16x2_rn(__uint_as_float(acc[2 * i]), __uint_as_float(acc[2 * i + 1]));
+  if (p.out_bf16 != nullptr) {
+    // row r's 64 bytes: piece j at r * 64 + 16 * (j ^ ((r >> 1) & 3))
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      st_smem_v4(stage + lane * 64 + 16 * (j ^ ((lane >> 1) & 3)), hb[4 * j], hb[4 * j + 1], hb[4 * j + 2], hb[4 * j + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = 8 * i + (lane >> 2), j = lane & 3;
+      const uint4 v = ld_smem_v4(stage + r * 64 + 16 * (j ^ ((r >> 1) & 3)));
+      if (row0 + r < p.T) *reinterpret_cast<uint4*>(p.out_bf16 + (row0 + r) * p.ldo + col + 8 * j) = v;
+    }
+    __syncwarp();
+  }
+  if (p.z_q != nullptr) {
+    const uint32_t code = ue8m0_from_bf16_amax(amax_bf16x2_words(hb, 16));
+    const float s = ue8m0_inverse(code);
+    uint32_t qw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      qw[i] = e4m3x2(bf16_lo(hb[2 * i]) * s, bf16_hi(hb[2 * i]) * s) |
+              (e4m3x2(bf16_lo(hb[2 * i + 1]) * s, bf16_hi(hb[2 * i + 1]) * s) << 16);
+    // row r's 32 bytes: piece j at r * 32 + 16 * (j ^ ((r >> 2) & 1))
+    const int sw = (lane >> 2) & 1;
+    st_smem_v4(stage + lane * 32 + 16 * sw, qw[0], qw[1], qw[2], qw[3]);
+    st_smem_v4(stage + lane * 32 + 16 * (sw ^ 1), qw[4], qw[5], qw[6], qw[7]);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = 16 * i + (lane >> 1), j = lane & 1;
+      const uint4 v = ld_smem_v4(stage + r * 32 + 16 * (j ^ ((r >> 2) & 1)));
+      if (row0 + r < p.T) *reinterpret_cast<uint4*>(p.z_q + (row0 + r) * p.ldz + col + 16 * j) = v;
+    }
+    __syncwarp();
+    word |= code << (8 * (c & 3));
+    if ((c & 3) == 3) {
+      const int64_t row = row0 + lane;
+      const int64_t wi = (col - 96) >> 7;  // first column of this 4-group word / 128
+      if (p.z_sf_tl != nullptr)
+        *reinterpret_cast<uint32_t*>(p.z_sf_tl + tiled128x4_word_offset(row, wi, p.z_gp4)) = word;
+      if (p.z_sf_pk != nullptr && row < p.z_mp4)
+        *reinterpret_cast<uint32_t*>(p.z_sf_pk + (wi * p.z_mp4 + row) * 4) = word;
+      word = 0;
+    }
+  }
+}
+
 // scale byte 0 of a padding token row (t >= T) of the tiled / packed z scales
 __device__ __forceinline__ void epi_zero_scale(const KArgs& p, int64_t t, int64_t col) {
   if (p.z_q == nullptr || t >= p.z_mp128) return;
@@ -923,7 +985,8 @@ struct PairCfg {
   static constexpr int OFF_B = STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_PK = OFF_SF + STAGES * SF_BYTES;  // PK: STAGES x 512 B of packed words
-  static constexpr int OFF_BAR = OFF_PK + (PK ? STAGES * 512 : 0);
+  static constexpr int OFF_EPI = OFF_PK + (PK ? STAGES * 512 : 0);  // 2 KB staging per epilogue warp
+  static constexpr int OFF_BAR = OFF_EPI + 8 * 2048;
   // full, empty, scale atoms in TMEM (STAGES each), accf, acce, drain; PK: packed words landed
   // (this CTA) and both CTAs' atoms scattered (even CTA), STAGES each
   static constexpr int OFF_MISC = OFF_BAR + ((PK ? 5 : 3) * STAGES + 4) * 8;
@@ -1277,6 +1340,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16) + 128 * half;
     const uint32_t acce0 = mapa_shared(bar_acce, 0);
     const int ew = warp - 2;  // this warp's share of a partial slot and its ready flag
+    const uint32_t stage = sbase + C::OFF_EPI + ew * 2048;
     int ti = 0;
     for (int w = 0;; ++w, ++ti) {
       int t, g, nf, kb_lo, kb_hi;
@@ -1370,7 +1434,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                 a[4 * x + 3] = __float_as_uint(__uint_as_float(a[4 * x + 3]) + u[x].w);
               }
             }
-            epi_row_chunk(p, a, row, col0 + 32 * c, word, c);
+            epi_row_chunk_staged(p, a, row0 + 32 * q, lane, col0 + 32 * c, word, c, stage);
           }
           tc_fence_before();
           __syncwarp();
@@ -1427,7 +1491,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       if (row0 >= p.z_mp128) continue;  // this half of a ragged last pair tile holds no token
       uint32_t word = 0;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) epi_row_chunk(p, acc[c], row, col0 + 32 * c, word, c);
+      for (int c = 0; c < 4; ++c) epi_row_chunk_staged(p, acc[c], row0 + 32 * q, lane, col0 + 32 * c, word, c, stage);
     }
   }
   __syncwarp();
