@@ -243,12 +243,14 @@ MXQ_API mxq_status mxq_selftest_hold_sms(int64_t sm_pairs, int64_t hold_us, void
  * o_proj_mxfp8_from_bf16 -- the _o_proj pair fed by bf16 o ([KeepMXFP8] Pieces: the wo_a that
  * quantizes its activation in the kernel, "pre-quantized == in-kernel"; Purpose: no quantize
  * launch between the producer of o and its consumer). wo_a loads o as bf16 and quantizes each
- * stage's tile in shared memory with exactly the rule of mxfp8_quantize (its epilogue warps, idle
- * during the mainloop, do it), so there is no quantize launch for o either.
- *   - T <= 384: the tiles and K splits of o_proj_mxfp8's wo_a, so z, its scales, the bf16 z and
- *     out are bit-identical to mxfp8_quantize(o) followed by o_proj_mxfp8 (same workspace).
- *   - T > 384: wo_a runs as 128 x 128 tiles on single SMs (not o_proj_mxfp8's SM pairs); z is
- *     then the same up to the last bit of the bf16 rounding of some sums.
+ * stage's tile in shared memory with exactly the rule of mxfp8_quantize (its epilogue warps do
+ * it), so there is no quantize launch for o either. wo_a runs the tiles and K splits of
+ * o_proj_mxfp8's wo_a (swap-AB tiles up to 384 tokens, SM pairs beyond), so z, its scales, the
+ * bf16 z and out are bit-identical to mxfp8_quantize(o) followed by o_proj_mxfp8 (same
+ * workspace). (Na not a multiple of 256 with T > 384: 128 x 128 tiles on single SMs, and z the
+ * same up to the last bit of the bf16 rounding of some sums.) It saves time at small T only
+ * (decode); from about 64 tokens on, the standalone quantizer followed by o_proj_mxfp8 is faster,
+ * because every feature tile of a group quantizes the same o tile again.
  *   o_bf16 : bf16 [T, G * Ka], row stride ld_o elements (ld_o * 2 a multiple of 16 bytes).
  * Other arguments as in o_proj_mxfp8 (the workspace serves wo_b).
  */

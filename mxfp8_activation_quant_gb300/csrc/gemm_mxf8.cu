@@ -220,11 +220,9 @@ __device__ __forceinline__ void epi_row_chunk(const KArgs& p, const uint32_t (&a
 // a warp's whole 32 x 128 share of the last tile in the idle operand stages, for 128- and 256-byte
 // rows, was no faster. The 16-byte pieces of a staged row are XOR-swizzled by the row, so that
 // neither the staging stores nor the loads conflict on banks. Every lane of the warp calls it.
-__device__ __forceinline__ void epi_row_chunk_staged(const KArgs& p, const uint32_t (&acc)[32], int64_t row0, int lane,
-                                                     int64_t col, uint32_t& word, int c, uint32_t stage) {
-  uint32_t hb[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) hb[i] = bf16x2_rn(__uint_as_float(acc[2 * i]), __uint_as_float(acc[2 * i + 1]));
+// (hb: the chunk already rounded to bf16, two columns per word)
+__device__ __forceinline__ void epi_hb_chunk_staged(const KArgs& p, const uint32_t (&hb)[16], int64_t row0, int lane,
+                                                    int64_t col, uint32_t& word, int c, uint32_t stage) {
   if (p.out_bf16 != nullptr) {
     // row r's 64 bytes: piece j at r * 64 + 16 * (j ^ ((r >> 1) & 3))
 #pragma unroll
@@ -270,6 +268,14 @@ __device__ __forceinline__ void epi_row_chunk_staged(const KArgs& p, const uint3
       word = 0;
     }
   }
+}
+
+__device__ __forceinline__ void epi_row_chunk_staged(const KArgs& p, const uint32_t (&acc)[32], int64_t row0, int lane,
+                                                     int64_t col, uint32_t& word, int c, uint32_t stage) {
+  uint32_t hb[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) hb[i] = bf16x2_rn(__uint_as_float(acc[2 * i]), __uint_as_float(acc[2 * i + 1]));
+  epi_hb_chunk_staged(p, hb, row0, lane, col, word, c, stage);
 }
 
 // scale byte 0 of a padding token row (t >= T) of the tiled / packed z scales
@@ -958,8 +964,6 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
 }
 
-constexpr int kThreadsP = 320;  // the pair kernel's warps 0..9 (warp 10 is added below)
-
 // ------------------------------------------------------------------------------------------
 // CTA-pair persistent kernel (large T). One tcgen05 MMA of M = 256 tokens x N = 256 features
 // spans the two CTAs of a cluster (cta_group::2). Each CTA streams its own 128 token rows and
@@ -972,41 +976,49 @@ constexpr int kThreadsP = 320;  // the pair kernel's warps 0..9 (warp 10 is adde
 // PK: the activation (A) scales arrive int32-packed MN-major: each stage's 128 words of this
 // CTA's token rows land in a staging slot on a barrier of the CTA's own, and warp 10 of each CTA
 // scatters them into the A atom before the even CTA copies the atoms into TMEM.
-template <int STAGES, bool PK = false>
+template <int STAGES, bool PK = false, bool CV = false>
 struct PairCfg {
-  static constexpr int A_BYTES = BM * BK;   // this CTA's 128 token rows
+  static constexpr int A_BYTES = BM * BK;   // this CTA's 128 token rows (E4M3)
+  // CV: the A slot receives the 128 x 128 bf16 tile (256-byte rows, no swizzle) and its first
+  // 16 KB are overwritten with the E4M3 tile the MMAs read
+  static constexpr int A_SLOT = CV ? 2 * A_BYTES : A_BYTES;
   static constexpr int B_BYTES = 128 * BK;  // this CTA's 128 of the 256 weight rows
   static constexpr int SF_BYTES = 512 * 3;  // scale atoms: A (own rows), B (both 128-row atoms)
   // bytes of one stage of both CTAs (counted on the even CTA's barrier) for a tile of n features
-  // (with PK the A atoms are not among them: the packed words complete on each CTA's own barrier)
+  // (with PK the A atoms are not among them: the packed words complete on each CTA's own barrier;
+  // with CV neither the A tile nor its atom: the bf16 tile completes on each CTA's own barrier)
   __host__ __device__ static constexpr uint32_t tx_bytes(int n) {
-    return 2u * (A_BYTES + (n / 2) * BK + (PK ? 0 : 512) + (n / 128) * 512);
+    return CV ? 2u * ((n / 2) * BK + (n / 128) * 512) : 2u * (A_BYTES + (n / 2) * BK + (PK ? 0 : 512) + (n / 128) * 512);
   }
-  static constexpr int OFF_B = STAGES * A_BYTES;
+  static constexpr int OFF_B = STAGES * A_SLOT;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_PK = OFF_SF + STAGES * SF_BYTES;  // PK: STAGES x 512 B of packed words
   static constexpr int OFF_EPI = OFF_PK + (PK ? STAGES * 512 : 0);  // 2 KB staging per epilogue warp
   static constexpr int OFF_BAR = OFF_EPI + 8 * 2048;
   // full, empty, scale atoms in TMEM (STAGES each), accf, acce, drain; PK: packed words landed
-  // (this CTA) and both CTAs' atoms scattered (even CTA), STAGES each
-  static constexpr int OFF_MISC = OFF_BAR + ((PK ? 5 : 3) * STAGES + 4) * 8;
+  // (this CTA) and both CTAs' atoms scattered (even CTA), STAGES each; CV: bf16 tile landed (this
+  // CTA), read by the 8 converting warps (this CTA), quantized by both CTAs (even CTA)
+  static constexpr int OFF_MISC = OFF_BAR + ((PK ? 5 : CV ? 6 : 3) * STAGES + 4) * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int SF_COLS = 16;
   static constexpr int TMEM_COLS = 512;  // 256 accumulator columns + STAGES x 16 scale columns
   static_assert(256 + STAGES * SF_COLS <= TMEM_COLS, "TMEM");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+  static_assert(!(PK && CV), "one activation form");
 };
 
 constexpr int kThreadsPair = 352;  // warp 0 TMA, 1 MMA, 2..9 epilogue, 10 scale copies
 
 // SK: the stream-K tail (p.sk_part / p.sk_flag / p.sk_ticket set); a separate instantiation keeps the
 // whole-tile kernel's code exactly as without it. PK: int32-packed activation scales (PairCfg).
-template <int STAGES, bool SK, bool PK = false>
+// CV: bf16 activations, quantized in the kernel (whole tiles only; see the converting epilogue).
+template <int STAGES, bool SK, bool PK = false, bool CV = false>
 __global__ void __launch_bounds__(kThreadsPair, 1)
     gemm_mxf8_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __grid_constant__ CUtensorMap tm_b64, const __grid_constant__ CUtensorMap tm_sfa,
                    const __grid_constant__ CUtensorMap tm_sfb, const KArgs p) {
-  using C = PairCfg<STAGES, PK>;
+  static_assert(!(CV && SK), "the converting kernel runs whole tiles");
+  using C = PairCfg<STAGES, PK, CV>;
   constexpr int BN = 256;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sraw = smem_u32(smem_raw);
@@ -1020,11 +1032,14 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   const uint32_t bar_sf = bar_accf + 24;             // STAGES x 8 B: scale atoms of a stage in TMEM
   const uint32_t bar_pk = bar_sf + STAGES * 8;       // PK: STAGES x 8 B, packed words landed (own)
   const uint32_t bar_scat = bar_pk + STAGES * 8;     // PK: STAGES x 8 B, both atoms scattered (even CTA)
+  const uint32_t bar_abf = bar_sf + STAGES * 8;      // CV: STAGES x 8 B, bf16 tile landed (own)
+  const uint32_t bar_rd = bar_abf + STAGES * 8;      // CV: STAGES x 8 B, the 8 converting warps have read it
+  const uint32_t bar_cvt = bar_rd + STAGES * 8;      // CV: STAGES x 8 B, both CTAs quantized (even CTA)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   int* issued_cnt = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
   int* consumed_cnt = reinterpret_cast<int*>(smem + C::OFF_MISC + 12);
-  int* scattered_cnt = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);  // PK
+  int* scattered_cnt = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);  // PK; CV: bf16 tiles quantized
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0 issues the MMAs
   const bool leader = rank == 0;
@@ -1121,6 +1136,12 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         mbar_init(bar_pk + 8 * s, 1);
         mbar_init(bar_scat + 8 * s, 2);  // warp 10 of each CTA
       }
+    if (CV)
+      for (int s = 0; s < STAGES; ++s) {
+        mbar_init(bar_abf + 8 * s, 1);
+        mbar_init(bar_rd + 8 * s, 8);    // the epilogue warps of this CTA
+        mbar_init(bar_cvt + 8 * s, 16);  // the epilogue warps of both CTAs
+      }
     *abort_flag = 0;
     *issued_cnt = 0;
     *consumed_cnt = 0;
@@ -1156,7 +1177,13 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       // PK: this CTA's token rows that exist in the packed array (rows >= Mp have no word)
       const int64_t pk_rows = PK ? (p.act_mp4 - a_row < 0 ? 0 : (p.act_mp4 - a_row < BM ? p.act_mp4 - a_row : BM)) : 0;
       auto load_act = [&](int s, int kb, uint32_t fb) {
-        tma_load_2d_pair(sbase + s * C::A_BYTES, &tm_a, fb, static_cast<int32_t>(a_x + kb * BK), static_cast<int32_t>(a_row));
+        if (CV) {  // the bf16 tile, on this CTA's own barrier: this CTA's epilogue warps quantize it
+          mbar_arrive_expect_tx(bar_abf + 8 * s, 2u * C::A_BYTES);
+          tma_load_2d(sbase + s * C::A_SLOT, &tm_a, bar_abf + 8 * s, static_cast<int32_t>(a_x + kb * BK),
+                      static_cast<int32_t>(a_row));
+          return;
+        }
+        tma_load_2d_pair(sbase + s * C::A_SLOT, &tm_a, fb, static_cast<int32_t>(a_x + kb * BK), static_cast<int32_t>(a_row));
         if (!PK) {
           tma_load_2d_pair(sbase + C::OFF_SF + s * C::SF_BYTES, &tm_sfa, fb, 0, static_cast<int32_t>(a_atom + kb));
         } else if (pk_rows > 0) {
@@ -1231,7 +1258,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           tc_fence_after();
           const uint32_t sfa_t = tmem + BN + s * C::SF_COLS;
           const uint32_t sfb_t = sfa_t + 4;
-          const uint64_t ad = sdesc_kmajor_sw128(sbase + s * C::A_BYTES);
+          const uint64_t ad = sdesc_kmajor_sw128(sbase + s * C::A_SLOT);
           const uint64_t bd = sdesc_kmajor_sw128(sbase + C::OFF_B + s * C::B_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
@@ -1307,6 +1334,33 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       }
     }
     if (lane == 0) *scattered_cnt = it;
+  } else if (warp == 10 && CV) {
+    // ---------------- scale copies once both CTAs have quantized the stage (even CTA) --------
+    if (leader && lane == 0) {
+      int it = 0;
+      for (int w = 0; !*abort_flag; ++w) {
+        int t, g, nf, kb_lo, kb_hi;
+        int64_t m0, n0;
+        if (!seg(w, t, g, m0, n0, nf, kb_lo, kb_hi)) break;
+        const bool full_tile = nf == BN;
+        for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait_bounded(bar_full + 8 * s, ph) || !mbar_wait_bounded(bar_cvt + 8 * s, ph)) {
+            *abort_flag = 1;
+            report_timeout(p.status);
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sf_src = sbase + C::OFF_SF + s * C::SF_BYTES;
+          const uint32_t sfa_t = tmem + BN + s * C::SF_COLS;
+          tc_cp_sf_atom_pair(sfa_t, sdesc_sf_atom(sf_src));
+          tc_cp_sf_atom_pair(sfa_t + 4, sdesc_sf_atom(sf_src + 512));
+          if (full_tile) tc_cp_sf_atom_pair(sfa_t + 8, sdesc_sf_atom(sf_src + 1024));
+          tc_commit_pair(bar_sf + 8 * s, 0x1);
+        }
+      }
+    }
   } else if (warp == 10) {
     // ---------------- scale copies (even CTA) ----------------
     if (leader && lane == 0) {
@@ -1333,6 +1387,123 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         }
       }
     }
+  } else if (warp >= 2 && CV) {
+    // ---------------- quantize the bf16 A tiles in place, and the epilogue (both CTAs) ---------
+    // The 8 epilogue warps quantize every stage of bf16 activations as mxfp8_quantize does: warp
+    // ew takes token rows [16 ew, 16 ew + 16) of the CTA's 128, lane l the 16-byte piece l % 16
+    // (8 elements) of row 2 j + l / 16 in step j, so that a load instruction covers two whole
+    // 256-byte rows; a 32-element group is 4 consecutive lanes (two xor-shuffles for its amax),
+    // a scale word 16 lanes. The E4M3 row r (128 bytes, 128-byte swizzle) overwrites bytes of
+    // bf16 row r / 2, so every warp reads all its rows first and waits until the other 7 have
+    // read theirs. The stages of a tile are quantized before its accumulator is waited for; the
+    // first stages of the next tile between the chunks of this tile's epilogue, so that the
+    // MMAs of the next tile (which may start once the accumulator has been read) find them.
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int ew = warp - 2;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16) + 128 * half;
+    const uint32_t acce0 = mapa_shared(bar_acce, 0);
+    const uint32_t cvt0 = mapa_shared(bar_cvt, 0);
+    const uint32_t stage = sbase + C::OFF_EPI + ew * 2048;
+    const int pc = lane & 15;
+    auto convert = [&](int i) -> bool {
+      const int s = i % STAGES;
+      const uint32_t ph = (i / STAGES) & 1;
+      if (!mbar_wait_bounded(bar_abf + 8 * s, ph)) return false;
+      const uint32_t slot = sbase + s * C::A_SLOT;
+      uint4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = ld_smem_v4(slot + (16 * ew + 2 * j + (lane >> 4)) * 256 + pc * 16);
+      uint2 qv[8];
+      uint32_t wd[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t amax = absmax8(v[j]);
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const uint32_t code = ue8m0_from_bf16_amax(amax);
+        qv[j] = quant8(v[j], ue8m0_inverse(code));
+        wd[j] = code | (__shfl_down_sync(0xffffffffu, code, 4) << 8) | (__shfl_down_sync(0xffffffffu, code, 8) << 16) |
+                (__shfl_down_sync(0xffffffffu, code, 12) << 24);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_rd + 8 * s);
+      if (!mbar_wait_bounded(bar_rd + 8 * s, ph)) return false;
+      const uint32_t atom = sbase + C::OFF_SF + s * C::SF_BYTES;  // A atom: first in the slot
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = 16 * ew + 2 * j + (lane >> 4);
+        st_smem_v2(slot + r * 128 + (((pc >> 1) ^ (r & 7)) << 4) + 8 * (pc & 1), qv[j].x, qv[j].y);
+        if (pc == 0) st_smem_u32(atom + (r & 31) * 16 + (r >> 5) * 4, wd[j]);
+      }
+      fence_proxy_async_smem();  // the MMAs and the scale copy read these through the async proxy
+      __syncwarp();
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(bar_cvt + 8 * s);
+        else
+          mbar_arrive_remote(cvt0 + 8 * s);
+      }
+      return true;
+    };
+    int ti = 0, cit = 0, it_end = 0;
+    bool ok = true;
+    for (int w = 0; ok; ++w, ++ti) {
+      int t, g, nf, kb_lo, kb_hi;
+      int64_t m0, n0;
+      if (!seg(w, t, g, m0, n0, nf, kb_lo, kb_hi)) break;
+      it_end += kb_hi - kb_lo;
+      while (ok && cit < it_end)
+        if ((ok = convert(cit))) ++cit;
+      if (ok && !mbar_wait_bounded(bar_accf, ti & 1)) ok = false;
+      if (!ok) {
+        *abort_flag = 1;
+        report_timeout(p.status);
+        break;
+      }
+      if (__any_sync(0xffffffffu, *abort_flag)) break;
+      tc_fence_after();
+      const bool cols = 128 * half < nf;  // a 128-feature item has no columns for half 1
+      uint32_t hb[4][16];
+      if (cols) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t a[32];
+          tmem_ld_x32(t_lane + 32 * c, a);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) hb[c][i] = bf16x2_rn(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {  // the MMA warp may overwrite this half of the accumulator now
+        if (leader)
+          mbar_arrive(bar_acce);
+        else
+          mbar_arrive_remote(acce0);
+      }
+      int nxt = 0;  // stages of the next tile quantized between this epilogue's chunks
+      {
+        int t1, g1, nf1, kl1, kh1;
+        int64_t m1, n1;
+        if (seg(w + 1, t1, g1, m1, n1, nf1, kl1, kh1)) nxt = kh1 - kl1 < 4 ? kh1 - kl1 : 4;
+      }
+      const int64_t row0 = m0 + BM * rank;
+      const bool live = cols && row0 < p.z_mp128;  // (this half of a ragged last pair tile holds no token)
+      const int64_t col0 = static_cast<int64_t>(g) * p.n_feat + n0 + 128 * half;
+      uint32_t word = 0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (live) epi_hb_chunk_staged(p, hb[c], row0 + 32 * q, lane, col0 + 32 * c, word, c, stage);
+        if (c < nxt && ok && (ok = convert(cit))) ++cit;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        report_timeout(p.status);
+      }
+    }
+    if (ew == 0 && lane == 0) *scattered_cnt = cit;
   } else if (warp >= 2) {
     // ---------------- epilogue (both CTAs) ----------------
     const int q = warp & 3;            // TMEM lane quarter
@@ -1505,6 +1676,13 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     if (*abort_flag || peer_abort)
       for (int i = *scattered_cnt; i < *issued_cnt; ++i)
         (void)mbar_wait_bounded(bar_pk + 8 * (i % STAGES), (i / STAGES) & 1);
+  }
+  if (CV && warp == 0 && lane == 0) {
+    // bf16 tiles this CTA loaded but its epilogue warps did not quantize: let them land first
+    const int peer_abort = ld_dsmem_s32(mapa_shared(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u));
+    if (*abort_flag || peer_abort)
+      for (int i = *scattered_cnt; i < *issued_cnt; ++i)
+        (void)mbar_wait_bounded(bar_abf + 8 * (i % STAGES), (i / STAGES) & 1);
   }
   if (leader && warp == 0 && lane == 0) {
     const int peer_abort = ld_dsmem_s32(mapa_shared(smem_u32(const_cast<int*>(abort_flag)), 1));
@@ -1780,15 +1958,15 @@ int pair_clusters_resident() {
 }
 
 // CTA-pair persistent launch: clusters of two, one CTA per SM, pair tiles of 256 x 256
-template <int STAGES, bool PK = false>
+// CV: bf16 activations quantized in the kernel; whole tiles, the same tiles and order as the
+// MXFP8-input launch of the shape (which takes the split tail only for more than 32 k-blocks per
+// tile), so that the sums are those of mxfp8_quantize followed by the MXFP8-input GEMM.
+template <int STAGES, bool PK = false, bool CV = false>
 cudaError_t launch_pair(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
-  using C = PairCfg<STAGES, PK>;
-  auto kern = gemm_mxf8_pair<STAGES, false, PK>;
-  auto kern_sk = gemm_mxf8_pair<STAGES, true, PK>;
+  using C = PairCfg<STAGES, PK, CV>;
+  auto kern = gemm_mxf8_pair<STAGES, false, PK, CV>;
   static const cudaError_t attr_err = set_smem_attrs(kern, C::SMEM_BYTES);
   if (attr_err != cudaSuccess) return attr_err;
-  static const cudaError_t attr_err_sk = set_smem_attrs(kern_sk, C::SMEM_BYTES);
-  if (attr_err_sk != cudaSuccess) return attr_err_sk;
   ka.splits = 1;
   ka.kb_per_cta = l.k_len / BK;
   const int64_t tiles = static_cast<int64_t>(l.G) * ceil_div(l.T, 2 * BM) * (l.n_feat / 256);
@@ -1804,7 +1982,11 @@ cudaError_t launch_pair(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
   // available.) Whole tiles take floor(tiles / P) waves plus half a tile (the last wave split in
   // two halves) or a whole one; measured: wo_b (64 k-blocks) gains at 1024..4096 tokens, wo_a
   // (32 k-blocks) never does.
+  if constexpr (!CV) {
   if (l.workspace != nullptr && tiles % max_pairs != 0) {
+    auto kern_sk = gemm_mxf8_pair<STAGES, true, PK>;
+    static const cudaError_t attr_err_sk = set_smem_attrs(kern_sk, C::SMEM_BYTES);
+    if (attr_err_sk != cudaSuccess) return attr_err_sk;
     const int resident = pair_clusters_resident<STAGES, PK>();
     const int sk_pairs = resident < max_pairs ? resident : max_pairs;
     const int64_t rem = sk_pairs > 0 ? tiles % sk_pairs : 0;
@@ -1822,12 +2004,15 @@ cudaError_t launch_pair(const GemmLaunch& l, KArgs ka, cudaStream_t stream) {
       kern = kern_sk;
     }
   }
+  }
   CUtensorMap tma_act, tma_wt, tma_wt64, tma_sfa, tma_sfb;
-  if (!make_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, BM)) return cudaErrorInvalidValue;
+  if (CV ? !make_bf16_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, BM) : !make_map(&tma_act, l.act, l.T, l.act_cols, l.act_ld, BM))
+    return cudaErrorInvalidValue;
   if (!make_map(&tma_wt, l.wt, static_cast<int64_t>(l.G) * l.n_feat, l.k_len, l.wt_ld, 128)) return cudaErrorInvalidValue;
   if (!make_map(&tma_wt64, l.wt, static_cast<int64_t>(l.G) * l.n_feat, l.k_len, l.wt_ld, 64)) return cudaErrorInvalidValue;
-  // (with packed activation scales the A atoms are not loaded through this map)
-  if (!make_sf_map(&tma_sfa, PK ? l.wt_sf : l.act_sf, PK ? 1 : ceil_div(l.T, 128) * ka.act_gp4)) return cudaErrorInvalidValue;
+  // (with packed activation scales or bf16 activations the A atoms are not loaded through this map)
+  if (!make_sf_map(&tma_sfa, PK || CV ? l.wt_sf : l.act_sf, PK || CV ? 1 : ceil_div(l.T, 128) * ka.act_gp4))
+    return cudaErrorInvalidValue;
   if (!make_sf_map(&tma_sfb, l.wt_sf, ceil_div(static_cast<int64_t>(l.G) * l.n_feat, 128) * ka.wt_gp4))
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
@@ -1899,6 +2084,7 @@ cudaError_t launch_gemm(const GemmLaunch& l, cudaStream_t stream) {
     if (l.T <= 64) return launch_swap<64, 2, B, 4>(l, ka, stream);
     if (l.T <= 128) return launch_swap<128, 3, B, 6>(l, ka, stream);
     if (l.T <= kSwapMaxTokens) return launch_swap<128, 3, B, 3>(l, ka, stream);
+    if (l.n_feat % 256 == 0) return launch_pair<4, false, true>(l, ka, stream);
     return launch_normal<128, 3, B>(l, ka, stream);
   }
   if (l.act_sf_packed) {  // int32-packed activation scales, moved into atoms in the kernel
