@@ -162,8 +162,9 @@ MXQ_API mxq_status rmsnorm_dual_out(const void* x_bf16, const void* gamma_bf16, 
  * (16-byte aligned). It must be zero-filled before its first use; every call that completes
  * leaves its flags and tickets zero again, so it needs no clearing between calls (after a call
  * that reported MXQ_ERR_TIMEOUT, zero it again). Calls that overlap in time (different streams)
- * need separate workspaces; calls ordered on one stream may share one, including both GEMMs of
- * o_proj_mxfp8. NULL workspace: whole tiles per pair, no partials.
+ * need separate workspaces; calls ordered on one stream may share one. Within o_proj_mxfp8 and
+ * o_proj_mxfp8_from_bf16 it serves wo_b alone (a programmatic dependent launch that overlaps
+ * wo_a's end). NULL workspace: whole tiles per pair, no partials.
  */
 MXQ_API int64_t mxq_workspace_bytes(void);
 
@@ -214,7 +215,9 @@ MXQ_API mxq_status gemm_mxfp8_bf16(const mxq_mx_tensor* a, const mxq_mx_tensor* 
  *   out = wo_b( MXFP8( RNE_bf16( einsum(o, wa) ) ) )
  * Two kernel launches, no standalone quantize launch. Arguments as in the two calls above;
  * z_q / z_sf_128x4 are required (the hand-off buffers), z_sf_packed_i32 and z_bf16 optional.
- * out_bf16 : [T, Nb], row stride Nb. Requires Nb % 128 == 0. One workspace serves both GEMMs.
+ * out_bf16 : [T, Nb], row stride Nb. Requires Nb % 128 == 0. The workspace serves wo_b (wo_a,
+ *            whose dependent wo_b may start before it ends, runs whole tiles): the call equals
+ *            wo_a_einsum_mxfp8 without a workspace followed by gemm_mxfp8_bf16 with it.
  */
 MXQ_API mxq_status o_proj_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, const mxq_mx_tensor* wb,
                                 int64_t T, int32_t G, int32_t Na, int32_t Ka, int32_t Nb, void* z_q,

@@ -277,8 +277,11 @@ mxq_status o_proj_mxfp8(const mxq_mx_tensor* o, const mxq_mx_tensor* wa, const m
   if (st != MXQ_OK) return st;
   if (!al16(out_bf16)) return MXQ_ERR_MISALIGNED;
   if ((st = check_workspace(workspace, workspace_bytes)) != MXQ_OK) return st;
-  st = wo_a_impl(o, wa, T, G, Na, Ka, z_q, z_sf_128x4, z_sf_packed_i32, z_bf16, workspace, workspace_bytes, status,
-                 stream, true);
+  // The workspace serves wo_b only. wo_b is a programmatic dependent of wo_a and its epilogue
+  // warps take split-tail tickets before wo_a has finished, so the two must not share the flags
+  // and tickets; wo_a gains nothing from the split anyway (a tile of 32 k-blocks never pays for
+  // it, and with more k-blocks measured slower).
+  st = wo_a_impl(o, wa, T, G, Na, Ka, z_q, z_sf_128x4, z_sf_packed_i32, z_bf16, nullptr, 0, status, stream, true);
   if (st != MXQ_OK) return st;
   const mxq_mx_tensor z = {z_q, z_sf_128x4, MXQ_SF_TILED_128X4, T, Kb, Kb};
   return gemm_impl(&z, wb, T, Nb, Kb, out_bf16, Nb, workspace, workspace_bytes, status, stream, true);

@@ -184,6 +184,37 @@ def test_split_k_grouped_fused_epilogue(mxq, oracle):
     assert torch.equal(zq.body, zq_w.body) and torch.equal(ztl.body, ztl_w.body) and torch.equal(zb.body, zb_w.body)
 
 
+def test_o_proj_workspace_serves_wo_b_only(mxq):
+    """At a shape where wo_a alone takes the split tail (G = 2, 2560 features, 8192 deep, T = 1000:
+    80 tiles of 64 k-blocks) and so does wo_b (80 tiles of 40 k-blocks), o_proj_mxfp8 gives the
+    workspace to wo_b only: wo_b, a programmatic dependent, takes its tickets while wo_a may still
+    run, so the two must not share flags. The call equals wo_a_einsum_mxfp8 without a workspace
+    followed by gemm_mxfp8_bf16 with it, byte for byte, and the flags end at zero."""
+    T, G, Na, Ka, Nb = 1000, 2, 2560, 8192, 5120
+    rng = np.random.default_rng(41)
+    O = gpu_mx(mxq, int_matrix(rng, T, G * Ka, -3, 3))
+    WA = gpu_mx(mxq, int_matrix(rng, G * Na, Ka, -3, 3))
+    WB = gpu_mx(mxq, int_matrix(rng, Nb, G * Na, -2, 2))
+    ws = torch.zeros(mxq.workspace_bytes(), dtype=torch.uint8, device="cuda")
+
+    def bufs():
+        return (torch.empty((T, G * Na), dtype=torch.uint8, device="cuda"), mxq.empty_sf(2, T, G * Na),
+                torch.empty((T, Nb), dtype=torch.bfloat16, device="cuda"))
+
+    st = mxq.new_status()
+    a = bufs()
+    for _ in range(3):  # repeated calls reuse the flags and tickets
+        mxq.o_proj_mxfp8(O, WA, WB, T, G, Na, Ka, Nb, a[0], a[1], a[2], status=st, workspace=ws)
+    b = bufs()
+    mxq.wo_a_einsum_mxfp8(O, WA, T, G, Na, Ka, z_q=b[0], z_sf_128x4=b[1], status=st, workspace=False)
+    mxq.gemm_mxfp8_bf16(mxq.MXFP8(b[0], b[1]), WB, b[2], status=st, workspace=ws)
+    torch.cuda.synchronize()
+    mxq.check_status(st)
+    assert _flags_zero(mxq, ws) and _slots_written(ws)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
 def test_split_k_o_proj_deterministic(mxq, weights):
     """The pair at T = 1000 (wo_b split, wo_a in whole tiles) repeats its bytes exactly, stays
     within one bf16 rounding of the whole-tile result, and leaves the flags zero."""
