@@ -530,11 +530,13 @@ def test_fused_chain_launches_two_kernels(mxq, weights, T):
 
 
 @pytest.mark.parametrize("T,pad", [(1, 0), (2, 0), (4, 0), (7, 64), (16, 0), (17, 0), (33, 64), (100, 0), (129, 0),
-                                   (256, 0), (300, 64), (384, 0), (385, 0), (1000, 64), (4096, 0), (8193, 0)])
+                                   (256, 0), (300, 64), (384, 0), (385, 0), (1000, 64), (2048, 0), (4096, 0),
+                                   (8193, 0)])
 def test_o_proj_from_bf16_matches_prequantized(mxq, oracle, weights, T, pad):
     """wo_a quantizing bf16 o in the kernel against mxfp8_quantize(o) followed by o_proj_mxfp8
     (the pages' "pre-quantized == in-kernel"). At every token count both run the same tiles and K
-    splits (swap-AB bands up to 384 tokens, the CTA-pair kernel beyond, quantizing in place): z,
+    splits (swap-AB bands up to 384 tokens, the CTA-pair kernel beyond, quantizing in place; at
+    2048 tokens its last wave runs in 256 x 128 halves): z,
     both scale layouts, the bf16 z and out are the same bytes. The in-kernel path also meets the
     oracle chain's tolerances (bf16 z within 4e-3, out within 1e-2; sampled rows beyond 384
     tokens). `pad` extra columns make o a strided view."""
