@@ -483,6 +483,7 @@ def _o_proj_fused_unfused(mxq, timer, c, T, WA, WB):
 SWEEP_O_PROJ_T = [1, 16, 64, 128, 256, 384, 512, 4096, 32768]
 SWEEP_QUANT_T = [4096, 32768]
 SWEEP_RMS_T = [1024, 4096, 8192]
+SWEEP_F2_T = [64, 1024, 8192]
 
 
 def compact_sweep(mxq, synth, torch, dev, WA, WB):
@@ -539,6 +540,27 @@ def compact_sweep(mxq, synth, torch, dev, WA, WB):
                    "frac_hbm": round(b / us / 1e3 / hbm, 4), "frac_nominal": round(b / us / 1e3 / NOMINAL_HBM_GBS, 4)})
         del xr, yr, yrq, sf
     res["rmsnorm_dual_out"] = rm
+    # the second producer -> consumer pair: RMSNorm's MXFP8 y fed straight into the MXFP8 GEMM
+    # (fused_wqa_wkv stand-in, 5120 -> synth.WQKV_N), against quantizing RMSNorm's bf16 y with a
+    # standalone launch before the same GEMM
+    wqq, wqs = mxq.quantize(synth.wqa_wkv_weight(0, device=dev), layouts=(2,))
+    wq = mxq.MXFP8(wqq, wqs[2])
+    f2 = []
+    for T in SWEEP_F2_T:
+        xr = synth.rmsnorm_input(0, T, device=dev)
+        gm = synth.rmsnorm_gamma(0, device=dev)
+        yr = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        yrq = torch.empty((T, H), dtype=torch.uint8, device=dev)
+        sf = mxq.empty_sf(2, T, H, dev)
+        yq2 = torch.empty_like(yrq)
+        sf2 = mxq.empty_sf(2, T, H, dev)
+        out = torch.empty((T, synth.WQKV_N), dtype=torch.bfloat16, device=dev)
+        chain = timer(lambda: (mxq.rmsnorm_dual_out(xr, gm, synth.RMS_EPS, yr, yrq, sf_128x4=sf),
+                               mxq.gemm_mxfp8_bf16(mxq.MXFP8(yrq, sf), wq, out)))
+        quant = timer(lambda: mxq.mxfp8_quantize(yr, yq2, None, None, sf2))
+        f2.append({"T": T, "rmsnorm_then_gemm_us": round(chain, 2), "standalone_quantize_of_y_us": round(quant, 2)})
+        del xr, yr, yrq, sf, yq2, sf2, out
+    res["rmsnorm_to_mxfp8_gemm"] = {"gemm": f"{H} -> {synth.WQKV_N}", "rows": f2}
     n = 8192
     A = mxq.MXFP8(*_rand_mx(mxq, synth, n, n, synth.TID_SQ_A, dev))
     B = mxq.MXFP8(*_rand_mx(mxq, synth, n, n, synth.TID_SQ_B, dev))
