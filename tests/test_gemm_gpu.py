@@ -570,6 +570,44 @@ def test_o_proj_from_bf16_matches_prequantized(mxq, oracle, weights, T, pad):
     assert rel_fro(bits_to_f64(bf16_bits(a[4]))[rows], out_ref) <= 1e-2
 
 
+@pytest.mark.parametrize("T,G,Na,Ka,Nb", [(600, 2, 512, 1024, 256), (700, 2, 384, 512, 256), (50, 3, 256, 384, 128)])
+def test_o_proj_from_bf16_other_shapes(mxq, oracle, T, G, Na, Ka, Nb):
+    """The bf16-o pair away from the DeepSeek shapes, with exact integer operands: (600, Na = 512)
+    runs the quantizing CTA-pair kernel with every tile in 256 x 128 halves, (700, Na = 384) the
+    one-CTA normal-orientation kernel, (50) a swap-AB band with 3 groups. bf16 z equals the
+    rounded exact product; the MXFP8 z and its scales equal the standalone quantizer applied to
+    that z; and where the tiles are o_proj_mxfp8's (Na a multiple of 256, or T <= 384) every
+    output is the bytes of mxfp8_quantize + o_proj_mxfp8."""
+    rng = np.random.default_rng(T + G + Na)
+    o = int_matrix(rng, T, G * Ka, -3, 3)
+    wa = int_matrix(rng, G * Na, Ka, -3, 3)
+    wb = int_matrix(rng, Nb, G * Na, -2, 2)
+    WA, WB = gpu_mx(mxq, wa), gpu_mx(mxq, wb)
+    st = mxq.new_status()
+
+    def bufs():
+        return (torch.empty((T, G * Na), dtype=torch.uint8, device="cuda"), mxq.empty_sf(2, T, G * Na),
+                torch.empty((T, G * Na), dtype=torch.bfloat16, device="cuda"),
+                torch.empty((T, Nb), dtype=torch.bfloat16, device="cuda"))
+
+    a = bufs()
+    mxq.o_proj_mxfp8_from_bf16(o.cuda(), WA, WB, T, G, Na, Ka, Nb, a[0], a[1], a[3], z_bf16=a[2], status=st)
+    torch.cuda.synchronize()
+    mxq.check_status(st)
+    od, wad = o.double().numpy(), wa.double().numpy()
+    exact = np.concatenate([od[:, g * Ka:(g + 1) * Ka] @ wad[g * Na:(g + 1) * Na].T for g in range(G)], axis=1)
+    assert np.array_equal(bf16_bits(a[2]), oracle.bf16_round(exact))
+    q2, sfs = mxq.quantize(a[2], layouts=(2,))
+    torch.cuda.synchronize()
+    assert torch.equal(q2, a[0]) and torch.equal(sfs[2], a[1])
+    if Na % 256 == 0 or T <= 384:
+        b = bufs()
+        mxq.o_proj_mxfp8(gpu_mx(mxq, o), WA, WB, T, G, Na, Ka, Nb, b[0], b[1], b[3], z_bf16=b[2], status=st)
+        torch.cuda.synchronize()
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+
+
 @pytest.mark.parametrize("T,N,K", [(1, 256, 512), (17, 256, 512), (40, 128, 1024), (100, 5120, 8192),
                                    (128, 256, 2048), (300, 256, 1024), (513, 256, 512), (700, 384, 512),
                                    (1000, 5120, 8192)])
